@@ -1,0 +1,306 @@
+"""fp64 CPU oracle of the Stable LatentMoE feed-forward layer (forward pass).
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module.  The CUDA library never calls it and shares no code with it; the two
+meet only in the seeded input bytes of ``lmoe_inputs``.
+
+What it computes, step by step in the pages' order and notation
+(Kimi K3 card "Latent mixture of experts", equations under "All 23 steps",
+and the ``KimiSparseMoeBlock.forward`` / ``moe_infer`` excerpt of
+modeling_kimi_linear.py; Kimi K2 card "Mixture of experts", "All 19 steps"):
+
+  router      z = x W_r,  s = sigma(z),  E_sel = top_k(s + b),
+              G_i = scale * s_i E_sel_i / sum_j s_j E_sel_j
+  latent down x^c = x W_down                          (K3 only)
+  expert i    g = x^c W_gate, u = x^c W_up, h = SiTU(g, u), E_i = h W_down
+  sum         u = sum_i G_i E_i                        (in the latent for K3)
+  norm        u_hat = RMSNorm(u)                       (K3, before the up-projection)
+  latent up   y_routed = u_hat W_up                    (K3 only)
+  shared      y_shared = SiTU-GLU(x) (full width)      (SwiGLU for K2)
+  output      Delta = y_routed + y_shared              (no residual inside the layer)
+
+Everything runs in float64 on weights dequantised exactly from their stored
+formats.  numpy's matmul serves as the one library primitive.
+
+Readings of points the pages leave open (each listed in the design doc):
+  * top-k ties go to the lower expert index; a token whose k-th and
+    (k+1)-th biased scores differ by less than 1e-6 is flagged, and either
+    choice there is correct;
+  * no epsilon in the renormalisation (every sigma > 0);
+  * RMSNorm(u) = w * u / sqrt(mean(u^2) + eps), eps from the config;
+  * SiTU: beta_1 = 4 caps the gate's linear factor, beta_2 = 25 caps the
+    up branch, gate = first projection, up = second;
+  * MXFP4 nibble order: the even K index sits in the low nibble;
+  * FP8 blocks are 128 (out) x 128 (in), w = e4m3(q) * scale.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TIE_EPS = 1e-6
+
+
+# ------------------------------------------------------------------ formats
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 stored as uint16 bit patterns -> float64 (exact)."""
+    b = np.asarray(bits).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def e2m1_value(nib: np.ndarray) -> np.ndarray:
+    """E2M1 (OCP MX FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit.
+    exponent 0 is subnormal: 0.5 * m; otherwise 2^(e-1) * (1 + m/2)."""
+    nib = np.asarray(nib).astype(np.int64)
+    sign = np.where(nib & 0x8, -1.0, 1.0)
+    e = (nib >> 1) & 0x3
+    m = (nib & 0x1).astype(np.float64)
+    mag = np.where(e == 0, 0.5 * m, np.exp2(e.astype(np.float64) - 1.0) * (1.0 + 0.5 * m))
+    return sign * mag
+
+
+def e8m0_value(s: np.ndarray) -> np.ndarray:
+    """E8M0 scale byte -> 2^(s - 127).  (0xFF is NaN in the format and is
+    never produced by the input generator.)"""
+    return np.exp2(np.asarray(s).astype(np.float64) - 127.0)
+
+
+def dequant_mxfp4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """codes uint8 [N, K/2] (even K in the low nibble) and E8M0 scales
+    uint8 [N, K/32] -> float64 [N, K]."""
+    q = np.asarray(q)
+    N, Kh = q.shape
+    K = 2 * Kh
+    nib = np.empty((N, K), dtype=np.uint8)
+    nib[:, 0::2] = q & 0x0F
+    nib[:, 1::2] = q >> 4
+    w = e2m1_value(nib)
+    return w * np.repeat(e8m0_value(s), 32, axis=1)[:, :K]
+
+
+def e4m3_value(b: np.ndarray) -> np.ndarray:
+    """OCP FP8 E4M3 (fn variant): 1 sign, 4 exponent (bias 7), 3 mantissa;
+    exponent 0 is subnormal m/8 * 2^-6; S.1111.111 is NaN."""
+    b = np.asarray(b).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, np.exp2(e.astype(np.float64) - 7.0) * (1.0 + m / 8.0))
+    mag = np.where((e == 15) & ((b & 7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def dequant_fp8_block128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """E4M3 bytes [N, K] and fp32 scales [ceil(N/128), ceil(K/128)] -> float64."""
+    q = np.asarray(q)
+    N, K = q.shape
+    scale = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), 128, 0), 128, 1)[:N, :K]
+    return e4m3_value(q) * scale
+
+
+# ------------------------------------------------------------ activations
+def sigmoid(z):
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-np.asarray(z, dtype=np.float64)))
+
+
+def situ(g, u, beta=4.0, linear_beta=25.0):
+    """SiTU-GLU (Kimi K3 card, routed-expert steps; SituAndMul):
+    a = beta * tanh(g / beta) * sigma(g);  u_bar = linear_beta * tanh(u / linear_beta);
+    h = a * u_bar."""
+    a = beta * np.tanh(g / beta) * sigmoid(g)
+    ubar = linear_beta * np.tanh(u / linear_beta)
+    return a * ubar
+
+
+def swiglu(g, u):
+    """Kimi K2 card, routed-expert steps: a = g * sigma(g), h = a * u."""
+    return g * sigmoid(g) * u
+
+
+def rms_norm(u, w, eps):
+    """RMSNorm over the last axis: w * u / sqrt(mean(u^2) + eps)."""
+    return w * u / np.sqrt(np.mean(u * u, axis=-1, keepdims=True) + eps)
+
+
+# ---------------------------------------------------------------- routing
+def route_from_logits(z: np.ndarray, bias: np.ndarray, k: int, scale: float = 1.0):
+    """Router steps after the logits.  z fp64 [T, E], bias [E].
+
+    Returns dict: idx [T, k] (by biased score descending, ties to the lower
+    index), G [T, k] (raw sigmoid renormalised over the selection, times
+    `scale`), s, c (= s + b), and flag [T] (k-th and (k+1)-th biased scores
+    within TIE_EPS)."""
+    z = np.asarray(z, dtype=np.float64)
+    T, E = z.shape
+    s = sigmoid(z)
+    c = s + np.asarray(bias, dtype=np.float64)[None, :]
+    idx = np.empty((T, k), dtype=np.int64)
+    flag = np.zeros(T, dtype=bool)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-c[t, e], e))
+        idx[t] = order[:k]
+        if k < E:
+            flag[t] = (c[t, order[k - 1]] - c[t, order[k]]) < TIE_EPS
+    G = weights_for(s, idx, scale)
+    return dict(idx=idx, G=G, s=s, c=c, flag=flag, z=z)
+
+
+def weights_for(s: np.ndarray, idx: np.ndarray, scale: float = 1.0) -> np.ndarray:
+    """G_i = scale * s_i / sum_{j in selection} s_j (raw sigmoid, not s + b)."""
+    sel = np.take_along_axis(s, idx, axis=1)
+    return scale * sel / sel.sum(axis=1, keepdims=True)
+
+
+def router(x: np.ndarray, Wr: np.ndarray, bias: np.ndarray, k: int, scale: float = 1.0):
+    """z = x W_r^T with W_r in nn.Linear [E, d] storage, then route."""
+    return route_from_logits(x @ Wr.T, bias, k, scale)
+
+
+def dispatch(idx: np.ndarray, E: int):
+    """Token -> expert dispatch of moe_infer, written as a counting sort.
+
+    The flattened assignment a = t*k + j goes to expert idx[t, j].  Returns
+    counts [E], offsets [E+1] (exclusive prefix sum), perm [T*k] (assignments
+    grouped by expert, in increasing a inside each expert) and inv [T*k]
+    (position of assignment a in perm)."""
+    flat = np.asarray(idx).reshape(-1)
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    fill = offsets[:-1].copy()
+    perm = np.empty(flat.size, dtype=np.int64)
+    inv = np.empty(flat.size, dtype=np.int64)
+    for a, e in enumerate(flat):
+        perm[fill[e]] = a
+        inv[a] = fill[e]
+        fill[e] += 1
+    return dict(counts=counts, offsets=offsets, perm=perm, inv=inv)
+
+
+# ------------------------------------------------------------- the layer
+class Layer:
+    """Weights of one layer instance in fp64, dequantised on first use.
+
+    W maps the C-ABI weight names to numpy arrays: bf16 tensors as uint16 bit
+    patterns, expert codes / scales as uint8 [E, N, K/2] / [E, N, K/32]
+    (MXFP4) or uint8 [E, N, K] / fp32 [E, N/128, K/128] (FP8).  Instead of
+    stacked arrays, W may carry ``expert_fn(name, e) -> (q, s)`` to fetch one
+    expert at a time."""
+
+    def __init__(self, cfg, W: dict):
+        self.cfg = cfg
+        self.W = W
+        self._cache = {}
+
+    def dense(self, name):
+        if name not in self._cache:
+            self._cache[name] = bf16_bits_to_f64(self.W[name])
+        return self._cache[name]
+
+    def expert(self, name, e):
+        key = (name, e)
+        if key not in self._cache:
+            if "expert_fn" in self.W:
+                q, s = self.W["expert_fn"](name, e)
+            else:
+                q, s = self.W[name + "_q"][e], self.W[name + "_s"][e]
+            if self.cfg.expert_wfmt == "mxfp4":
+                self._cache[key] = dequant_mxfp4(q, s)
+            else:
+                self._cache[key] = dequant_fp8_block128(q, s)
+        return self._cache[key]
+
+    def shared(self, name):
+        if self.cfg.expert_wfmt == "mxfp4":
+            return self.dense(name)
+        key = (name, "fp8")
+        if key not in self._cache:
+            self._cache[key] = dequant_fp8_block128(self.W[name], self.W[name + "_s"])
+        return self._cache[key]
+
+    def act(self, g, u):
+        c = self.cfg
+        if c.act == "situ":
+            return situ(g, u, c.situ_beta, c.situ_linear_beta)
+        return swiglu(g, u)
+
+
+def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
+            idx: np.ndarray | None = None) -> dict:
+    """Delta for the tokens in x (bf16 bits [T, d]).
+
+    routes: a dict from `router` to reuse; idx: a given selection [T, k]
+    (its G is recomputed from this run's raw sigmoid).  Returns Delta and
+    the intermediates."""
+    cfg = layer.cfg
+    x = bf16_bits_to_f64(x_bits)
+    T = x.shape[0]
+    k = cfg.top_k
+    if routes is None:
+        routes = router(x, layer.dense("router_w"), layer.W["router_bias"], k, cfg.routed_scale)
+    if idx is not None:
+        routes = dict(routes)
+        routes["idx"] = np.asarray(idx, dtype=np.int64)
+        routes["G"] = weights_for(routes["s"], routes["idx"], cfg.routed_scale)
+    sel, G = routes["idx"], routes["G"]
+
+    # Latent down-projection (K3); the K2 experts take x itself.
+    xe = x @ layer.dense("w_down_latent").T if cfg.d_latent else x
+
+    # moe_infer: group the assignments by expert, run each selected expert once
+    # on its tokens, put the outputs back in assignment order.
+    disp = dispatch(sel, cfg.n_experts)
+    out = np.zeros((T * k, xe.shape[1]), dtype=np.float64)
+    for e in range(cfg.n_experts):
+        lo, hi = disp["offsets"][e], disp["offsets"][e + 1]
+        if hi == lo:
+            continue
+        assign = disp["perm"][lo:hi]
+        toks = assign // k
+        g = xe[toks] @ layer.expert("ex_gate", e).T
+        u = xe[toks] @ layer.expert("ex_up", e).T
+        h = layer.act(g, u)
+        out[assign] = h @ layer.expert("ex_down", e).T
+    # Weighted sum over each token's selection (u in the pages' notation).
+    u_sum = (out.reshape(T, k, -1) * G[:, :, None]).sum(axis=1)
+
+    if cfg.d_latent:
+        u_hat = rms_norm(u_sum, layer.dense("norm_w"), cfg.norm_eps) if cfg.use_latent_norm else u_sum
+        y_routed = u_hat @ layer.dense("w_up_latent").T
+    else:
+        u_hat = None
+        y_routed = u_sum
+
+    if cfg.d_shared_ff:
+        gs = x @ layer.shared("sh_gate").T
+        us = x @ layer.shared("sh_up").T
+        h_s = layer.act(gs, us)
+        y_shared = h_s @ layer.shared("sh_down").T
+    else:
+        h_s = None
+        y_shared = np.zeros_like(y_routed)
+    delta = y_routed + y_shared
+    return dict(delta=delta, routes=routes, xc=xe if cfg.d_latent else None, u=u_sum,
+                u_hat=u_hat, y_routed=y_routed, y_shared=y_shared, h_s=h_s, dispatch=disp)
+
+
+# ------------------------------------------------------- input conversion
+def numpy_inputs(tensors: dict) -> dict:
+    """torch tensors from lmoe_inputs -> numpy arrays the oracle reads
+    (bf16 as uint16 bit patterns).  Only the representation changes."""
+    import torch
+    out = {}
+    for k, v in tensors.items():
+        if not isinstance(v, torch.Tensor):
+            out[k] = v
+            continue
+        v = v.detach().cpu()
+        if v.dtype == torch.bfloat16:
+            out[k] = v.view(torch.int16).numpy().view(np.uint16)
+        else:
+            out[k] = v.numpy()
+    return out
