@@ -1,0 +1,181 @@
+/*
+ * lmoe — forward pass of the Stable LatentMoE feed-forward layer on one
+ * GB300 (sm_103a).  C ABI: plain pointers and sizes, no C++ or torch types.
+ *
+ * What the layer computes (Kimi K3 card "Latent mixture of experts", the
+ * equations under "All 23 steps" and the KimiSparseMoeBlock.forward /
+ * moe_infer excerpt of modeling_kimi_linear.py; Kimi K2 card "Mixture of
+ * experts", "All 19 steps"):
+ *
+ *   z = x W_r^T,  s = sigmoid(z),  S = top_k(s + b)
+ *   G_i = routed_scale * s_i / sum_{j in S} s_j       (raw s, not s + b)
+ *   x^c = x W_down^T                                   (latent layers only)
+ *   for i in S:  g = x^c W_gate,i^T,  u = x^c W_up,i^T,
+ *                h = SiTU(g, u) = b1 tanh(g/b1) sigmoid(g) * b2 tanh(u/b2)
+ *                (SwiGLU g sigmoid(g) u for LMOE_ACT_SWIGLU),  E_i = h W_down,i^T
+ *   u = sum_i G_i E_i,  u_hat = norm_w * u / sqrt(mean(u^2) + eps)
+ *   y_routed = u_hat W_up^T                            (latent layers only)
+ *   y_shared = SiTU-GLU of x with the shared weights (full width)
+ *   Delta = y_routed + y_shared                        (no residual added)
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers unless the name says host.  All
+ *     matrices are row-major in nn.Linear [out][in] storage (the input
+ *     dimension is contiguous).  bf16 values are raw IEEE bfloat16.
+ *   - Weights are BORROWED: the caller owns them, they must stay valid and
+ *     unchanged for the handle's lifetime, and the library never writes them.
+ *     The handle owns only its workspace, sized at create for max_tokens.
+ *   - Calls are stream-ordered and asynchronous unless stated.  Argument
+ *     errors are reported synchronously and nothing is launched.  An
+ *     asynchronous CUDA error or a kernel-side timeout surfaces on the next
+ *     call that checks (lmoe_sync_status, lmoe_forward_host).
+ *   - One handle is used by one stream at a time (the workspace is shared by
+ *     its calls).  `out` may not alias `x`.
+ *   - No call performs a host synchronisation except lmoe_create,
+ *     lmoe_destroy, lmoe_forward_host and lmoe_sync_status.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#if defined(__GNUC__)
+#define LMOE_API __attribute__((visibility("default")))
+#else
+#define LMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size, T > max_tokens */
+  LMOE_ERR_UNSUPPORTED = 2,  /* a configuration this build does not implement */
+  LMOE_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+  LMOE_ERR_OOM = 4,          /* workspace allocation failed */
+  LMOE_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired; results are invalid */
+} lmoe_status;
+
+typedef enum { LMOE_ACT_SITU = 0, LMOE_ACT_SWIGLU = 1 } lmoe_act;
+typedef enum { LMOE_W_MXFP4 = 0, LMOE_W_FP8_BLOCK128 = 1 } lmoe_wfmt;
+
+/* Layer shape and constants; keys mirror the model config (num_experts,
+ * num_experts_per_token, routed_expert_hidden_size, moe_intermediate_size,
+ * num_shared_experts x moe_intermediate_size, latent_moe_use_norm,
+ * rms_norm_eps, activation_situ_beta, activation_situ_linear_beta). */
+typedef struct {
+  int d_model;          /* d: 7168 for Kimi K3 / K2 */
+  int d_latent;         /* l: 3584 for K3; 0 = non-latent block (K2) */
+  int n_experts;        /* E: 896 (K3), 384 (K2) */
+  int top_k;            /* k: 16 (K3), 8 (K2); 1 <= k <= E */
+  int d_expert_ff;      /* routed expert hidden width: 3072 (K3), 2048 (K2) */
+  int d_shared_ff;      /* shared MLP hidden width: 6144 (K3, two experts merged); 0 = none */
+  int use_latent_norm;  /* 1: RMSNorm between the expert sum and the up-projection */
+  float norm_eps;       /* RMSNorm epsilon */
+  float routed_scale;   /* 1.0 (K3), 2.827 (K2) */
+  float situ_beta;      /* 4: cap of the gate's linear factor */
+  float situ_linear_beta; /* 25: cap of the up branch */
+  lmoe_act act;
+  lmoe_wfmt expert_wfmt;
+  int max_tokens;       /* largest T any call on this handle will pass */
+} lmoe_config;
+
+/* Layer weights (all device pointers, borrowed).
+ *   router_w       bf16 [E][d]                  router_bias  fp32 [E]
+ *   w_down_latent  bf16 [l][d]                  w_up_latent  bf16 [d][l]
+ *   norm_w         bf16 [l]                     (latent layers only)
+ *   ex_{gate,up}_q  MXFP4: uint8 [E][F][K/2], K = l (or d for K2): two E2M1
+ *                   codes per byte, even K index in the low nibble
+ *   ex_down_q       MXFP4: uint8 [E][l][F/2]
+ *   ex_*_s          MXFP4: E8M0 uint8 [E][N][K/32], one scale per 32 K values
+ *   (LMOE_W_FP8_BLOCK128: ex_*_q E4M3 uint8 [E][N][K], ex_*_s fp32
+ *    [E][ceil(N/128)][ceil(K/128)]; sh_* the same without E and sh_*_s set.)
+ *   sh_gate, sh_up bf16 [Fs][d]                 sh_down bf16 [d][Fs]
+ * Alignment: every pointer 16-byte aligned, code/scale arrays 32-byte. */
+typedef struct {
+  const void* router_w;
+  const float* router_bias;
+  const void* w_down_latent;
+  const void* w_up_latent;
+  const void* norm_w;
+  const uint8_t* ex_gate_q;
+  const uint8_t* ex_up_q;
+  const uint8_t* ex_down_q;
+  const void* ex_gate_s;
+  const void* ex_up_s;
+  const void* ex_down_s;
+  const void* sh_gate;
+  const void* sh_up;
+  const void* sh_down;
+  const void* sh_gate_s;
+  const void* sh_up_s;
+  const void* sh_down_s;
+} lmoe_weights;
+
+typedef struct lmoe_ctx* lmoe_handle;
+
+/* Validate the config and weights, allocate the workspace for max_tokens and
+ * encode the TMA descriptors of the weights.  Synchronises `stream`.
+ * Errors: INVALID_ARG (null pointers, bad shapes), UNSUPPORTED (shapes the
+ * kernels do not cover: d, l, F, Fs must be multiples of 32; E <= 2048;
+ * k <= 32; MXFP4 latent layers only in this build; the current device is
+ * not an sm_103 GPU), OOM, CUDA.  On error *out is NULL. */
+LMOE_API lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStream_t stream, lmoe_handle* out);
+
+/* Router only (Kimi K3 card, router steps; port notes item 3): topk_idx
+ * int32 [T][k], sorted by biased score s + b descending, exact ties to the
+ * lower expert index; topk_w fp32 [T][k] = routed_scale * s / sum s over
+ * the selection.  x: bf16 [T][d].  T = 0 is a no-op. */
+LMOE_API lmoe_status lmoe_route(lmoe_handle h, const void* x_bf16, int T, int32_t* topk_idx, float* topk_w,
+                       cudaStream_t stream);
+
+/* Whole layer: out bf16 [T][d] = Delta.  topk_idx_opt / topk_w_opt, when not
+ * NULL, receive the routing of lmoe_route.  T = 0 is a no-op. */
+LMOE_API lmoe_status lmoe_forward(lmoe_handle h, const void* x_bf16, int T, void* out_bf16, int32_t* topk_idx_opt,
+                         float* topk_w_opt, cudaStream_t stream);
+
+/* lmoe_forward on HOST buffers: copies x (bf16 [T][d], host memory; pinned
+ * for asynchronous copies) into the workspace, runs the layer and copies
+ * Delta back to out_host.  Synchronises `stream` before returning, so the
+ * host buffers may be reused at once.  Returns a deferred error, if any. */
+LMOE_API lmoe_status lmoe_forward_host(lmoe_handle h, const void* x_host, int T, void* out_host, cudaStream_t stream);
+
+/* Token -> expert dispatch alone (moe_infer's counting, argsort and
+ * grouping written as a counting sort): topk_idx int32 [T][k] in; counts
+ * int32 [E]; offsets int32 [E+1] (exclusive prefix sum of counts); perm
+ * int32 [T*k] = flattened assignments a = t*k + j grouped by expert, in
+ * increasing a inside each expert.  Indices outside [0, E) are an error
+ * the kernel reports through lmoe_sync_status (LMOE_ERR_INVALID_ARG). */
+LMOE_API lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, cudaStream_t stream);
+
+/* Copy an intermediate of the last lmoe_forward on this handle out of the
+ * workspace (stream-ordered): "logits" fp32 [T][E] (router z), "xc" fp32
+ * [T][l], "u" fp32 [T][l] (expert sum), "u_hat" bf16 [T][l], "h_shared"
+ * bf16 [T][Fs], "counts" int32 [E], "offsets" int32 [E+1], "perm" int32
+ * [T*k].  `bytes` must equal the tensor's size for the last T. */
+LMOE_API lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t stream);
+
+/* Synchronise `stream` and return the first deferred error: a CUDA error, a
+ * kernel timeout (TIMEOUT) or an out-of-range expert index (INVALID_ARG).
+ * Clears the kernel-side error flag. */
+LMOE_API lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t stream);
+
+/* Number of kernels the last lmoe_forward launched (for launch accounting). */
+LMOE_API int lmoe_last_launch_count(lmoe_handle h);
+
+/* Release the workspace.  Synchronises the device work of this handle.
+ * NULL is accepted. */
+LMOE_API lmoe_status lmoe_destroy(lmoe_handle h);
+
+/* Static string for a status code. */
+LMOE_API const char* lmoe_status_string(lmoe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMOE_H */

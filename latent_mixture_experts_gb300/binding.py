@@ -1,0 +1,211 @@
+"""ctypes binding of the lmoe C ABI (include/lmoe.h).
+
+Argument marshalling only: torch supplies device memory and the stream, every
+step of the layer runs in the library's CUDA kernels.  The binding fails
+loudly when the library is missing or no GPU is present; there is no CPU
+path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "liblmoe.so")
+
+LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_CUDA, LMOE_ERR_OOM, LMOE_ERR_TIMEOUT = range(6)
+LMOE_ACT_SITU, LMOE_ACT_SWIGLU = 0, 1
+LMOE_W_MXFP4, LMOE_W_FP8_BLOCK128 = 0, 1
+
+# Every symbol include/lmoe.h declares.
+EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lmoe_dispatch",
+           "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_destroy",
+           "lmoe_status_string")
+
+
+class LmoeConfig(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("d_latent", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("d_expert_ff", ctypes.c_int), ("d_shared_ff", ctypes.c_int),
+                ("use_latent_norm", ctypes.c_int), ("norm_eps", ctypes.c_float), ("routed_scale", ctypes.c_float),
+                ("situ_beta", ctypes.c_float), ("situ_linear_beta", ctypes.c_float), ("act", ctypes.c_int),
+                ("expert_wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int)]
+
+
+_WEIGHT_FIELDS = ("router_w", "router_bias", "w_down_latent", "w_up_latent", "norm_w", "ex_gate_q", "ex_up_q",
+                  "ex_down_q", "ex_gate_s", "ex_up_s", "ex_down_s", "sh_gate", "sh_up", "sh_down", "sh_gate_s",
+                  "sh_up_s", "sh_down_s")
+
+
+class LmoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load liblmoe.so (built by latent_mixture_experts_gb300.build).  Raises
+    if it is absent: nothing here falls back to another implementation."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"lmoe CUDA library not built: {path} missing "
+                               "(run python -m latent_mixture_experts_gb300.build)")
+        lib = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "lmoe_create": (I, [ctypes.POINTER(LmoeConfig), ctypes.POINTER(LmoeWeights), P, ctypes.POINTER(P)]),
+            "lmoe_route": (I, [P, P, I, P, P, P]),
+            "lmoe_forward": (I, [P, P, I, P, P, P, P]),
+            "lmoe_forward_host": (I, [P, P, I, P, P]),
+            "lmoe_dispatch": (I, [P, P, I, P, P, P, P]),
+            "lmoe_debug_tensor": (I, [P, ctypes.c_char_p, P, S, P]),
+            "lmoe_sync_status": (I, [P, P]),
+            "lmoe_last_launch_count": (I, [P]),
+            "lmoe_destroy": (I, [P]),
+            "lmoe_status_string": (ctypes.c_char_p, [I]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().lmoe_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(call: str, st: int):
+    if st != LMOE_OK:
+        raise LmoeError(call, st)
+
+
+def make_config(cfg, max_tokens: int) -> LmoeConfig:
+    """C config from an lmoe_inputs.LayerConfig-like object."""
+    return LmoeConfig(d_model=cfg.d_model, d_latent=cfg.d_latent, n_experts=cfg.n_experts, top_k=cfg.top_k,
+                      d_expert_ff=cfg.d_expert_ff, d_shared_ff=cfg.d_shared_ff,
+                      use_latent_norm=int(cfg.use_latent_norm), norm_eps=cfg.norm_eps,
+                      routed_scale=cfg.routed_scale, situ_beta=cfg.situ_beta,
+                      situ_linear_beta=cfg.situ_linear_beta,
+                      act=LMOE_ACT_SITU if cfg.act == "situ" else LMOE_ACT_SWIGLU,
+                      expert_wfmt=LMOE_W_MXFP4 if cfg.expert_wfmt == "mxfp4" else LMOE_W_FP8_BLOCK128,
+                      max_tokens=int(max_tokens))
+
+
+class LatentMoE:
+    """One layer instance on the current CUDA device.
+
+    weights: dict of CUDA tensors named as the C weight struct (bf16 tensors
+    as torch.bfloat16, codes/scales as torch.uint8, bias float32).  The
+    tensors are borrowed: this object keeps references so they outlive the
+    handle."""
+
+    def __init__(self, cfg, weights: dict, max_tokens: int, stream=None):
+        lib = load_library()
+        if not torch.cuda.is_available():
+            raise RuntimeError("lmoe needs a CUDA GPU; no CPU implementation exists")
+        self.cfg = cfg
+        self.max_tokens = int(max_tokens)
+        self._weights = {k: v for k, v in weights.items() if isinstance(v, torch.Tensor)}
+        for k, v in self._weights.items():
+            if not v.is_cuda or not v.is_contiguous():
+                raise ValueError(f"weight {k} must be a contiguous CUDA tensor")
+        w = LmoeWeights(**{n: (self._weights[n].data_ptr() if n in self._weights else None)
+                           for n in _WEIGHT_FIELDS})
+        c = make_config(cfg, max_tokens)
+        h = ctypes.c_void_p()
+        _check("lmoe_create", lib.lmoe_create(ctypes.byref(c), ctypes.byref(w), _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self._lib = lib
+
+    # -- calls mirroring the C ABI -------------------------------------
+    def lmoe_route(self, x: torch.Tensor, stream=None):
+        T = x.shape[0]
+        idx = torch.empty(T, self.cfg.top_k, dtype=torch.int32, device=x.device)
+        w = torch.empty(T, self.cfg.top_k, dtype=torch.float32, device=x.device)
+        _check("lmoe_route", self._lib.lmoe_route(self._h, _ptr(x), T, _ptr(idx), _ptr(w), _stream(stream)))
+        return idx, w
+
+    def lmoe_forward(self, x: torch.Tensor, out: torch.Tensor | None = None, return_routing: bool = False,
+                     stream=None):
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.cfg.d_model, dtype=torch.bfloat16, device=x.device)
+        idx = w = None
+        if return_routing:
+            idx = torch.empty(T, self.cfg.top_k, dtype=torch.int32, device=x.device)
+            w = torch.empty(T, self.cfg.top_k, dtype=torch.float32, device=x.device)
+        _check("lmoe_forward", self._lib.lmoe_forward(self._h, _ptr(x), T, _ptr(out), _ptr(idx), _ptr(w),
+                                                      _stream(stream)))
+        return (out, idx, w) if return_routing else out
+
+    def lmoe_forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None):
+        _check("lmoe_forward_host", self._lib.lmoe_forward_host(self._h, _ptr(x_host), x_host.shape[0],
+                                                                _ptr(out_host), _stream(stream)))
+        return out_host
+
+    def lmoe_dispatch(self, topk_idx: torch.Tensor, stream=None):
+        T = topk_idx.shape[0]
+        E = self.cfg.n_experts
+        counts = torch.empty(E, dtype=torch.int32, device=topk_idx.device)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=topk_idx.device)
+        perm = torch.empty(T * self.cfg.top_k, dtype=torch.int32, device=topk_idx.device)
+        _check("lmoe_dispatch", self._lib.lmoe_dispatch(self._h, _ptr(topk_idx), T, _ptr(counts), _ptr(offsets),
+                                                        _ptr(perm), _stream(stream)))
+        return counts, offsets, perm
+
+    def lmoe_debug_tensor(self, name: str, T: int, stream=None):
+        c = self.cfg
+        shapes = {"logits": ((T, c.n_experts), torch.float32), "xc": ((T, c.d_latent), torch.float32),
+                  "u": ((T, c.d_latent), torch.float32), "u_hat": ((T, c.d_latent), torch.bfloat16),
+                  "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "counts": ((c.n_experts,), torch.int32),
+                  "offsets": ((c.n_experts + 1,), torch.int32), "perm": ((T * c.top_k,), torch.int32)}
+        shape, dt = shapes[name]
+        dst = torch.empty(shape, dtype=dt, device="cuda")
+        _check("lmoe_debug_tensor", self._lib.lmoe_debug_tensor(self._h, name.encode(), _ptr(dst),
+                                                                dst.numel() * dst.element_size(), _stream(stream)))
+        return dst
+
+    def lmoe_sync_status(self, stream=None):
+        _check("lmoe_sync_status", self._lib.lmoe_sync_status(self._h, _stream(stream)))
+
+    def lmoe_last_launch_count(self) -> int:
+        return int(self._lib.lmoe_last_launch_count(self._h))
+
+    def lmoe_destroy(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check("lmoe_destroy", self._lib.lmoe_destroy(self._h))
+        self._h = None
+
+    # -- conveniences ----------------------------------------------------
+    forward = lmoe_forward
+    route = lmoe_route
+    dispatch = lmoe_dispatch
+    close = lmoe_destroy
+
+    def __del__(self):
+        try:
+            self.lmoe_destroy()
+        except Exception:
+            pass

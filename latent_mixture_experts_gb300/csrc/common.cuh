@@ -1,0 +1,90 @@
+// Device helpers shared by the layer's kernels: activations, number formats,
+// block scaling of activations into two E4M3 terms.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace lmoe {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// SiTU-GLU (Kimi K3 card, routed-expert steps): a = b1 tanh(g/b1) sigma(g),
+// u_bar = b2 tanh(u/b2), h = a * u_bar.  act == 1: SwiGLU g sigma(g) u
+// (Kimi K2 card, routed-expert steps).
+__device__ __forceinline__ float glu_act(float g, float u, int act, float b1, float b2) {
+  if (act == 1) return g * sigmoidf_(g) * u;
+  const float a = b1 * tanhf(g / b1) * sigmoidf_(g);
+  const float ub = b2 * tanhf(u / b2);
+  return a * ub;
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q), __NV_E4M3);
+  return __half2float(__half(h));
+}
+// 2^(e - 127) for an E8M0 byte e in [1, 254], built from its bit pattern.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) { return __uint_as_float(e << 23); }
+
+// E8M0 scale byte for a 32-element block whose largest magnitude is amax,
+// chosen so that amax / scale lands in [256, 512): the top binade of E4M3
+// (largest finite 448; values above it saturate).  Clamped so the scale and
+// its reciprocal stay normal floats.
+__device__ __forceinline__ uint32_t e4m3_block_scale(float amax) {
+  const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  int s = ef - 8;
+  s = s < 1 ? 1 : (s > 253 ? 253 : s);
+  return static_cast<uint32_t>(s);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Two-term E4M3 encoding of one element of a 32-element block held across
+// the 32 lanes of a warp: a ~= q_hi * 2^(s_hi-127) + q_lo * 2^(s_lo-127),
+// the second term quantising the first one's exact residual with its own
+// block scale.  Every lane gets its codes; all lanes get the two scales.
+struct HiLo {
+  uint8_t q_hi, q_lo;
+  uint32_t s_hi, s_lo;
+};
+__device__ __forceinline__ HiLo quant_hilo_warp(float a) {
+  HiLo r;
+  const float amax = warp_max(fabsf(a));
+  r.s_hi = e4m3_block_scale(amax);
+  r.q_hi = f32_to_e4m3(a * e8m0_to_f32(254u - r.s_hi));
+  const float res = a - e4m3_to_f32(r.q_hi) * e8m0_to_f32(r.s_hi);
+  const float rmax = warp_max(fabsf(res));
+  r.s_lo = e4m3_block_scale(rmax);
+  r.q_lo = f32_to_e4m3(res * e8m0_to_f32(254u - r.s_lo));
+  return r;
+}
+
+// Byte offset of one scale inside the tensor-memory staging image of a
+// 128-row (or 128-column) operand block: 32 lines of 16 bytes, line r0 holds
+// for c = 0..3 the four k-block scales of row 32c + r0.  This is the image
+// tcgen05.cp.32x128b.warpx4 replicates into the four lane quarters, where
+// the block-scaled MMA reads row n at lane n % 32, column n / 32, byte =
+// the k-block's scale id.
+__device__ __forceinline__ uint32_t sf_atom_offset(uint32_t n_in_128, uint32_t kb_in_4) {
+  return (n_in_128 & 31u) * 16u + (n_in_128 >> 5) * 4u + kb_in_4;
+}
+
+}  // namespace lmoe

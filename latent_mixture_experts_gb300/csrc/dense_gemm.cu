@@ -1,0 +1,227 @@
+// Dense bf16 GEMMs of the layer on the 5th-generation tensor cores:
+// router logits, latent down-projection, shared-expert gate/up, and the
+// K-concatenated [u_hat | h_shared] x [W_up ; W_shared_down] output GEMM.
+//
+// Weights are the MMA's A operand (M = 128 output features per tile) and
+// tokens the B operand (N = BN tokens): at decode the token count is small
+// and the weights are streamed once.  Operands arrive by TMA with 128-byte
+// swizzle into a multi-stage shared-memory ring; one thread issues
+// tcgen05.mma into a TMEM fp32 accumulator; all four warps read it back
+// with tcgen05.ld and store fp32 partial sums per K split.
+#include "common.cuh"
+#include "lmoe_internal.h"
+
+namespace lmoe {
+
+namespace {
+
+template <int BN>
+struct DenseCfg {
+  static constexpr int kA = 16384;             // 128 rows x 64 bf16
+  static constexpr int kB = BN * 128;          // BN rows x 64 bf16
+  static constexpr int kStage = kA + kB;
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 5 : 6);
+  static constexpr int kSmem = kStages * kStage + 1024;
+  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constant__ DenseParams p) {
+  using C = DenseCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  __shared__ uint64_t full[C::kStages], empty[C::kStages], done;
+  __shared__ uint32_t tmem_base;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, nt = blockIdx.y, sp = blockIdx.z;
+  const int seg = (p.mode == 1 && mt >= p.mtiles0) ? 1 : 0;
+  const int m0 = (seg ? mt - p.mtiles0 : mt) * 128;
+  const int Mseg = seg ? p.M1 : p.M0;
+  const int out_row0 = (seg ? p.M0 : 0) + m0;
+  const int n0 = nt * BN;
+  const int kb0 = static_cast<int>((static_cast<long long>(sp) * p.nkb) / p.splits);
+  const int kb1 = static_cast<int>((static_cast<long long>(sp + 1) * p.nkb) / p.splits);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    const CUtensorMap* am = seg ? &p.a1 : &p.a0;
+    tma_prefetch_desc(am);
+    tma_prefetch_desc(&p.b0);
+    for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+      const int s = i % C::kStages;
+      if (i >= C::kStages && !mbar_wait(&empty[s], ((i / C::kStages) - 1) & 1, p.err, kErrTimeout)) break;
+      const CUtensorMap* A = am;
+      const CUtensorMap* B = &p.b0;
+      int kc = kb * 64;
+      if (p.mode == 2 && kb >= p.nkb0) {
+        A = &p.a1;
+        B = &p.b1;
+        kc = (kb - p.nkb0) * 64;
+      }
+      uint8_t* st = sm + s * C::kStage;
+      mbar_arrive_expect_tx(&full[s], C::kStage);
+      tma_load_2d(st, A, &full[s], kc, m0);
+      tma_load_2d(st + C::kA, B, &full[s], kc, n0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(128, BN);
+    for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+      const int s = i % C::kStages;
+      if (!mbar_wait(&full[s], (i / C::kStages) & 1, p.err, kErrTimeout)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(sm + s * C::kStage);
+      const uint32_t b_addr = a_addr + C::kA;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_bf16(tacc, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k), idesc, (i | k) != 0);
+      mma_commit(&empty[s]);
+    }
+    mma_commit(&done);
+  }
+  __syncwarp();
+
+  // Epilogue: lane = output feature, column = token.
+  const bool ok = mbar_wait(&done, 0, p.err, kErrTimeout);
+  tc_fence_after();
+  const int row = m0 + 32 * warp + lane;
+  const bool row_ok = row < Mseg;
+  const bool have = ok && kb1 > kb0;
+  float* outp = p.out + static_cast<size_t>(sp) * p.T * p.ldo + out_row0 + 32 * warp + lane;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (n0 + c0 >= p.T) break;
+    uint32_t r[16];
+    tmem_ld16(tmem_addr(tacc, 32 * warp, c0), r);
+    tmem_ld_wait();
+    if (row_ok) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = n0 + c0 + j;
+        if (t < p.T) outp[static_cast<size_t>(t) * p.ldo] = have ? __uint_as_float(r[j]) : 0.0f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tacc, C::kTmemCols);
+}
+
+template <int BN>
+cudaError_t launch_bn(const DenseParams& p, int mtiles, cudaStream_t s) {
+  using C = DenseCfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(dense_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(mtiles, (p.T + BN - 1) / BN, p.splits);
+  dense_gemm_kernel<BN><<<grid, 128, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------- finalizers
+__global__ void finalize_sum_f32_kernel(const float* __restrict__ part, int splits, int T, int M, int ld,
+                                        float* __restrict__ out, int ldo) {
+  const size_t n = static_cast<size_t>(T) * M;
+  const size_t plane = static_cast<size_t>(T) * ld;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = i / M, m = i % M;
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[s * plane + t * ld + m];
+    out[t * ldo + m] = acc;
+  }
+}
+
+__global__ void finalize_sum_bf16_kernel(const float* __restrict__ part, int splits, int T, int M, int ld,
+                                         __nv_bfloat16* __restrict__ out, int ldo, const float* __restrict__ add,
+                                         int ld_add) {
+  const size_t n = static_cast<size_t>(T) * M;
+  const size_t plane = static_cast<size_t>(T) * ld;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = i / M, m = i % M;
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[s * plane + t * ld + m];
+    if (add) acc += add[t * ld_add + m];
+    out[t * ldo + m] = __float2bfloat16_rn(acc);
+  }
+}
+
+__global__ void finalize_glu_bf16_kernel(const float* __restrict__ part, int splits, int T, int F, int ld,
+                                         __nv_bfloat16* __restrict__ out, int act, float b1, float b2) {
+  const size_t n = static_cast<size_t>(T) * F;
+  const size_t plane = static_cast<size_t>(T) * ld;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = i / F, f = i % F;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      g += part[s * plane + t * ld + f];
+      u += part[s * plane + t * ld + F + f];
+    }
+    out[t * F + f] = __float2bfloat16_rn(glu_act(g, u, act, b1, b2));
+  }
+}
+
+int ew_grid(size_t n) {
+  size_t g = (n + 255) / 256;
+  return static_cast<int>(g < 152 * 16 ? (g ? g : 1) : 152 * 16);
+}
+
+}  // namespace
+
+cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s) {
+  switch (BN) {
+    case 32: return launch_bn<32>(p, mtiles, s);
+    case 64: return launch_bn<64>(p, mtiles, s);
+    case 128: return launch_bn<128>(p, mtiles, s);
+    case 256: return launch_bn<256>(p, mtiles, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,
+                                    cudaStream_t s) {
+  const size_t n = static_cast<size_t>(T) * M;
+  finalize_sum_f32_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, M, ld, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M, int ld, void* out, int ldo,
+                                     const float* add_opt, int ld_add, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(T) * M;
+  finalize_sum_bf16_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, M, ld,
+                                                     static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_glu_bf16(const float* part, int splits, int T, int F, int ld, void* out, int act,
+                                     float b1, float b2, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(T) * F;
+  finalize_glu_bf16_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, F, ld, static_cast<__nv_bfloat16*>(out),
+                                                     act, b1, b2);
+  return cudaGetLastError();
+}
+
+}  // namespace lmoe

@@ -1,0 +1,606 @@
+// C ABI of the Stable LatentMoE layer: handle, workspace, launch sequence.
+//
+// lmoe_forward, all on the caller's stream, no host synchronisation:
+//   1 router GEMM (bf16 tcgen05, fp32 split-K partial logits)
+//   2 top-k: sum partials, sigmoid, + bias, select, renormalise
+//   3 dispatch: counting sort into BN-row expert tiles (3 kernels)
+//   4 latent down-projection x^c = x W_down^T (+ split-K sum)
+//   5 x^c rows -> hi/lo E4M3 activations in expert-tile order
+//   6 grouped gate/up MXFP4 GEMM with SiTU epilogue -> hi/lo E4M3 h
+//   7 grouped down MXFP4 GEMM, epilogue x G_i -> per-assignment outputs
+//   8 slot-ordered sum + RMSNorm -> u_hat (bf16)
+//   9 shared gate/up GEMM (M-concatenated) + SiTU -> h_shared (bf16)
+//  10 [u_hat | h_shared] x [W_up ; W_shared_down] (K-concatenated) -> Delta
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/lmoe.h"
+#include "lmoe_internal.h"
+#include "tmap.h"
+
+using namespace lmoe;
+
+struct lmoe_ctx {
+  lmoe_config cfg;
+  lmoe_weights w;
+  int dev = 0, num_sms = 148;
+  int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
+  int Kp = 0, Fp = 0, MT_gu = 0, MT_dn = 0, KG_gu = 0, KG_dn = 0;
+  int Tm = 0, Pm = 0, Ppad = 0, max_tiles = 0, nchunks_max = 0;
+  // device memory
+  void* pool = nullptr;
+  size_t pool_bytes = 0;
+  int* err = nullptr;
+  float* part = nullptr;
+  float* xc = nullptr;
+  float* logits = nullptr;
+  int32_t* idx = nullptr;
+  float* G = nullptr;
+  int32_t *counts = nullptr, *offsets = nullptr, *tile_off = nullptr, *perm = nullptr, *inv_pad = nullptr;
+  int32_t *blockcnt = nullptr, *ntiles = nullptr;
+  int4* tiles = nullptr;
+  uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr;
+  float* y = nullptr;
+  float* u = nullptr;
+  void* u_hat = nullptr;
+  void* h_s = nullptr;
+  void* x_stage = nullptr;
+  void* out_stage = nullptr;
+  uint8_t *sfa_gate = nullptr, *sfa_up = nullptr, *sfa_down = nullptr;
+  const uint8_t *codes_gate = nullptr, *codes_up = nullptr, *codes_down = nullptr;
+  uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
+  // static tensor maps
+  CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd, m_exg, m_exu, m_exd;
+  int last_T = 0;
+  int last_launches = 0;
+};
+
+namespace {
+
+lmoe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return LMOE_OK;
+  if (e == cudaErrorMemoryAllocation) return LMOE_ERR_OOM;
+  return LMOE_ERR_CUDA;
+}
+#define LMOE_TRY(expr)                                   \
+  do {                                                   \
+    cudaError_t e_ = (expr);                             \
+    if (e_ != cudaSuccess) return cuda_status(e_);       \
+  } while (0)
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int dense_bn(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
+int moe_bn(int T, int k, int E) { return static_cast<long long>(T) * k <= 4LL * E ? 16 : 64; }
+
+// K splits of a dense GEMM: fill about one wave of CTAs, at least two
+// 64-wide k-blocks per split.
+int dense_splits(int mtiles, int ntiles, int nkb, int num_sms) {
+  const int tiles = mtiles * ntiles;
+  int s = num_sms / std::max(tiles, 1);
+  s = std::min(s, std::max(nkb / 2, 1));
+  return std::max(s, 1);
+}
+
+struct Carve {
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count, char* base) {
+    off = align_up(off, 1024);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+bool map_bf16(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, K, rows, static_cast<uint64_t>(K) * 2, 64, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_fp4(CUtensorMap* m, const void* base, int K, long long rows) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, base, K, rows, static_cast<uint64_t>(K) / 2, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_u8(CUtensorMap* m, const void* base, int K, long long rows, int box_rows) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, K, rows, K, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Largest (splits x T) a dense GEMM with `mtiles` and `nkb` needs for T <= Tm.
+long long max_split_rows(int mtiles, int nkb, int Tm, int num_sms) {
+  long long best = 0;
+  for (int T = 1; T <= Tm;) {
+    const int BN = dense_bn(T);
+    const int nt = ceil_div(T, BN);
+    const int s = dense_splits(mtiles, nt, nkb, num_sms);
+    const int Tend = std::min(Tm, nt * BN);   // same (BN, ntiles) up to here
+    best = std::max(best, static_cast<long long>(s) * Tend);
+    T = Tend + 1;
+  }
+  return best;
+}
+
+lmoe_status check_err(lmoe_ctx* h) {
+  int e[4] = {0, 0, 0, 0};
+  LMOE_TRY(cudaMemcpy(e, h->err, sizeof(e), cudaMemcpyDeviceToHost));
+  LMOE_TRY(cudaMemset(h->err, 0, sizeof(e)));
+  if (e[0]) return LMOE_ERR_TIMEOUT;
+  if (e[1]) return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& launches) {
+  const int BN = dense_bn(T);
+  DenseParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a0 = h->m_router;
+  if (!map_bf16(&p.b0, x, h->d, T, BN)) return LMOE_ERR_CUDA;
+  p.mode = 0;
+  p.M0 = h->E;
+  p.mtiles0 = ceil_div(h->E, 128);
+  p.T = T;
+  p.nkb = ceil_div(h->d, 64);
+  p.nkb0 = p.nkb;
+  p.splits = dense_splits(p.mtiles0, ceil_div(T, BN), p.nkb, h->num_sms);
+  p.ldo = h->E;
+  p.out = h->part;
+  p.err = h->err;
+  LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+  LMOE_TRY(launch_topk(h->part, p.splits, T, h->E, h->w.router_bias, h->k, h->cfg.routed_scale, h->idx, h->G,
+                       h->logits, st));
+  launches += 2;
+  return LMOE_OK;
+}
+
+lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, cudaStream_t st, int& launches) {
+  DispatchBufs b;
+  b.counts = counts;
+  b.offsets = offsets;
+  b.perm = perm;
+  b.inv_pad = h->inv_pad;
+  b.tile_off = h->tile_off;
+  b.blockcnt = h->blockcnt;
+  b.tiles = h->tiles;
+  b.ntiles = h->ntiles;
+  b.err = h->err;
+  LMOE_TRY(launch_dispatch(idx, T, h->k, h->E, BN, b, st));
+  launches += 3;
+  return LMOE_OK;
+}
+
+lmoe_status validate_cfg(const lmoe_config* c) {
+  if (c->d_model <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->d_expert_ff <= 0 || c->max_tokens <= 0 ||
+      c->d_latent < 0 || c->d_shared_ff < 0 || c->top_k > c->n_experts)
+    return LMOE_ERR_INVALID_ARG;
+  if (c->act != LMOE_ACT_SITU && c->act != LMOE_ACT_SWIGLU) return LMOE_ERR_INVALID_ARG;
+  if (c->expert_wfmt != LMOE_W_MXFP4 && c->expert_wfmt != LMOE_W_FP8_BLOCK128) return LMOE_ERR_INVALID_ARG;
+  if (c->expert_wfmt != LMOE_W_MXFP4 || c->d_latent == 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->d_model % 32 || c->d_latent % 32 || c->d_expert_ff % 32 || c->d_shared_ff % 32) return LMOE_ERR_UNSUPPORTED;
+  if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->max_tokens) * c->top_k > (1LL << 30)) return LMOE_ERR_UNSUPPORTED;
+  if (c->use_latent_norm && !(c->norm_eps >= 0.f)) return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
+  const void* need16[] = {w->router_w, w->router_bias, w->w_down_latent, w->w_up_latent};
+  for (const void* p : need16)
+    if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+  if (c->use_latent_norm && (!w->norm_w || !aligned(w->norm_w, 16))) return LMOE_ERR_INVALID_ARG;
+  const void* need32[] = {w->ex_gate_q, w->ex_up_q, w->ex_down_q, w->ex_gate_s, w->ex_up_s, w->ex_down_s};
+  for (const void* p : need32)
+    if (!p || !aligned(p, 32)) return LMOE_ERR_INVALID_ARG;
+  if (c->d_shared_ff) {
+    const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
+    for (const void* p : sh)
+      if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+  }
+  return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lmoe_status_string(lmoe_status s) {
+  switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LMOE_ERR_CUDA: return "CUDA error";
+    case LMOE_ERR_OOM: return "out of device memory";
+    case LMOE_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStream_t stream, lmoe_handle* out) {
+  if (!out) return LMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return LMOE_ERR_INVALID_ARG;
+  lmoe_status vs = validate_cfg(cfg);
+  if (vs != LMOE_OK) return vs;
+  vs = validate_weights(cfg, w);
+  if (vs != LMOE_OK) return vs;
+
+  int dev = 0;
+  LMOE_TRY(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  LMOE_TRY(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3) return LMOE_ERR_UNSUPPORTED;   // built for sm_103a only
+  if (!encode_tiled_fn()) return LMOE_ERR_CUDA;
+
+  lmoe_ctx* h = new (std::nothrow) lmoe_ctx();
+  if (!h) return LMOE_ERR_OOM;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->dev = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->d = cfg->d_model;
+  h->din = cfg->d_latent;
+  h->E = cfg->n_experts;
+  h->k = cfg->top_k;
+  h->F = cfg->d_expert_ff;
+  h->Fs = cfg->d_shared_ff;
+  h->Kp = static_cast<int>(align_up(h->din, 128));
+  h->Fp = static_cast<int>(align_up(h->F, 128));
+  h->MT_gu = h->Fp / 128;
+  h->MT_dn = ceil_div(h->din, 128);
+  h->KG_gu = h->Kp / 128;
+  h->KG_dn = h->Fp / 128;
+  h->Tm = cfg->max_tokens;
+  h->Pm = h->Tm * h->k;
+  const int bn_max = moe_bn(h->Tm, h->k, h->E);
+  h->Ppad = h->Pm + h->E * (bn_max - 1);
+  h->max_tiles = h->Pm / 16 + h->E + 1;
+  h->nchunks_max = ceil_div(h->Pm, kDispatchChunk);
+
+  // dense partial buffer: max over the four GEMMs of splits * T * ld
+  long long part_elems = 0;
+  {
+    const int nkb_d = ceil_div(h->d, 64);
+    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->E, 128), nkb_d, h->Tm, h->num_sms) * h->E);
+    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->din, 128), nkb_d, h->Tm, h->num_sms) * h->din);
+    if (h->Fs)
+      part_elems = std::max(part_elems,
+                            max_split_rows(2 * ceil_div(h->Fs, 128), nkb_d, h->Tm, h->num_sms) * 2LL * h->Fs);
+    const int nkb_o = ceil_div(h->din, 64) + (h->Fs ? ceil_div(h->Fs, 64) : 0);
+    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->d, 128), nkb_o, h->Tm, h->num_sms) * h->d);
+  }
+  const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
+  const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
+  const bool pad_gu = h->Kp != h->din, pad_dn = h->Fp != h->F;
+
+  auto carve = [&](char* base) {
+    Carve c;
+    h->err = c.take<int>(4, base);
+    h->part = c.take<float>(static_cast<size_t>(part_elems), base);
+    h->xc = c.take<float>(static_cast<size_t>(h->Tm) * h->din, base);
+    h->logits = c.take<float>(static_cast<size_t>(h->Tm) * h->E, base);
+    h->idx = c.take<int32_t>(h->Pm, base);
+    h->G = c.take<float>(h->Pm, base);
+    h->counts = c.take<int32_t>(h->E, base);
+    h->offsets = c.take<int32_t>(h->E + 1, base);
+    h->tile_off = c.take<int32_t>(h->E + 1, base);
+    h->perm = c.take<int32_t>(h->Pm, base);
+    h->inv_pad = c.take<int32_t>(h->Pm, base);
+    h->blockcnt = c.take<int32_t>(static_cast<size_t>(h->nchunks_max) * h->E, base);
+    h->ntiles = c.take<int32_t>(1, base);
+    h->tiles = c.take<int4>(h->max_tiles, base);
+    h->xq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Kp, base);
+    h->xsf = c.take<uint8_t>(xsf_bytes, base);
+    h->hq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Fp, base);
+    h->hsf = c.take<uint8_t>(hsf_bytes, base);
+    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->din, base);
+    h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->din, base);
+    h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->din, base);
+    h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);
+    h->x_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
+    h->out_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
+    h->sfa_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_gu * h->KG_gu * 512, base);
+    h->sfa_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_gu * h->KG_gu * 512, base);
+    h->sfa_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_dn * h->KG_dn * 512, base);
+    if (pad_gu) {
+      h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
+      h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
+    }
+    if (pad_dn) h->pad_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->din * (h->Fp / 2), base);
+    return c.off;
+  };
+  h->pool_bytes = carve(nullptr);
+  cudaError_t ae = cudaMalloc(&h->pool, h->pool_bytes);
+  if (ae != cudaSuccess) {
+    delete h;
+    return ae == cudaErrorMemoryAllocation ? LMOE_ERR_OOM : LMOE_ERR_CUDA;
+  }
+  carve(static_cast<char*>(h->pool));
+
+  auto fail = [&](lmoe_status s) {
+    cudaFree(h->pool);
+    delete h;
+    return s;
+  };
+  if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  // expert weights: scale atoms, K padding when a reduction dim is not a multiple of 128
+  const uint8_t* sg = static_cast<const uint8_t*>(w->ex_gate_s);
+  const uint8_t* su = static_cast<const uint8_t*>(w->ex_up_s);
+  const uint8_t* sd = static_cast<const uint8_t*>(w->ex_down_s);
+  if (launch_relayout_sfa(sg, h->E, h->F, h->din / 32, h->MT_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
+      launch_relayout_sfa(su, h->E, h->F, h->din / 32, h->MT_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
+      launch_relayout_sfa(sd, h->E, h->din, h->F / 32, h->MT_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess)
+    return fail(LMOE_ERR_CUDA);
+  h->codes_gate = w->ex_gate_q;
+  h->codes_up = w->ex_up_q;
+  h->codes_down = w->ex_down_q;
+  if (pad_gu) {
+    if (launch_pad_codes(w->ex_gate_q, h->E, h->F, h->din, h->Kp, h->pad_gate, stream) != cudaSuccess ||
+        launch_pad_codes(w->ex_up_q, h->E, h->F, h->din, h->Kp, h->pad_up, stream) != cudaSuccess)
+      return fail(LMOE_ERR_CUDA);
+    h->codes_gate = h->pad_gate;
+    h->codes_up = h->pad_up;
+  }
+  if (pad_dn) {
+    if (launch_pad_codes(w->ex_down_q, h->E, h->din, h->F, h->Fp, h->pad_down, stream) != cudaSuccess)
+      return fail(LMOE_ERR_CUDA);
+    h->codes_down = h->pad_down;
+  }
+  bool ok = true;
+  ok &= map_bf16(&h->m_router, w->router_w, h->d, h->E, 128);
+  ok &= map_bf16(&h->m_wdown, w->w_down_latent, h->d, h->din, 128);
+  ok &= map_bf16(&h->m_wup, w->w_up_latent, h->din, h->d, 128);
+  if (h->Fs) {
+    ok &= map_bf16(&h->m_shg, w->sh_gate, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shu, w->sh_up, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shd, w->sh_down, h->Fs, h->d, 128);
+  }
+  ok &= map_fp4(&h->m_exg, h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F);
+  ok &= map_fp4(&h->m_exu, h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F);
+  ok &= map_fp4(&h->m_exd, h->codes_down, h->Fp, static_cast<long long>(h->E) * h->din);
+  if (!ok) return fail(LMOE_ERR_CUDA);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  if (cudaGetLastError() != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  *out = h;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_destroy(lmoe_handle h) {
+  if (!h) return LMOE_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaFree(h->pool);
+  delete h;
+  return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+lmoe_status lmoe_route(lmoe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w, cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !aligned(x, 16) || !topk_idx || !topk_w) return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  lmoe_status s = run_router(h, x, T, st, launches);
+  if (s != LMOE_OK) return s;
+  const size_t n = static_cast<size_t>(T) * h->k;
+  LMOE_TRY(cudaMemcpyAsync(topk_idx, h->idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+  LMOE_TRY(cudaMemcpyAsync(topk_w, h->G, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!topk_idx || !counts || !offsets || !perm) return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  return run_dispatch(h, topk_idx, T, moe_bn(T, h->k, h->E), counts, offsets, perm, st, launches);
+}
+
+lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t* topk_idx_opt, float* topk_w_opt,
+                         cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !out || !aligned(x, 16) || !aligned(out, 16) || x == out) return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  const int d = h->d, din = h->din, Fs = h->Fs;
+  const int BN = dense_bn(T);
+  const int nt = ceil_div(T, BN);
+  const int nkb_d = ceil_div(d, 64);
+
+  // 1-2 router
+  lmoe_status s = run_router(h, x, T, st, launches);
+  if (s != LMOE_OK) return s;
+  // 3 dispatch
+  const int BNm = moe_bn(T, h->k, h->E);
+  s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
+  if (s != LMOE_OK) return s;
+
+  // 4 latent down-projection
+  {
+    DenseParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a0 = h->m_wdown;
+    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
+    p.mode = 0;
+    p.M0 = din;
+    p.mtiles0 = ceil_div(din, 128);
+    p.T = T;
+    p.nkb = nkb_d;
+    p.nkb0 = nkb_d;
+    p.splits = dense_splits(p.mtiles0, nt, nkb_d, h->num_sms);
+    p.ldo = din;
+    p.out = p.splits == 1 ? h->xc : h->part;
+    p.err = h->err;
+    LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+    ++launches;
+    if (p.splits > 1) {
+      LMOE_TRY(launch_finalize_sum_f32(h->part, p.splits, T, din, din, h->xc, din, st));
+      ++launches;
+    }
+  }
+  // 5 activations -> hi/lo E4M3 in expert-tile order
+  LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+  ++launches;
+  // 6-7 routed experts
+  {
+    MoeGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a_gate = h->m_exg;
+    p.a_up = h->m_exu;
+    if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
+    p.sfa_gate = h->sfa_gate;
+    p.sfa_up = h->sfa_up;
+    p.sfb = h->xsf;
+    p.tiles = h->tiles;
+    p.ntiles = h->ntiles;
+    p.perm = h->perm;
+    p.G = h->G;
+    p.err = h->err;
+    p.N_out = h->F;
+    p.MT = h->MT_gu;
+    p.KG = h->KG_gu;
+    p.hq = h->hq;
+    p.hsf = h->hsf;
+    p.Fp = h->Fp;
+    p.act = h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0;
+    p.b1 = h->cfg.situ_beta;
+    p.b2 = h->cfg.situ_linear_beta;
+    p.y = h->y;
+    LMOE_TRY(launch_moe_gate_up(p, BNm, h->num_sms, st));
+    ++launches;
+    MoeGemmParams q = p;
+    q.a_gate = h->m_exd;
+    if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
+    q.sfa_gate = h->sfa_down;
+    q.sfa_up = nullptr;
+    q.sfb = h->hsf;
+    q.N_out = din;
+    q.MT = h->MT_dn;
+    q.KG = h->KG_dn;
+    LMOE_TRY(launch_moe_down(q, BNm, h->num_sms, st));
+    ++launches;
+  }
+  // 8 expert sum in slot order + latent RMSNorm
+  LMOE_TRY(launch_combine_norm(h->y, T, h->k, din, h->w.norm_w, h->cfg.use_latent_norm, h->cfg.norm_eps, h->u,
+                               h->u_hat, st));
+  ++launches;
+  // 9 shared experts gate/up + SiTU
+  if (Fs) {
+    DenseParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a0 = h->m_shg;
+    p.a1 = h->m_shu;
+    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
+    p.mode = 1;
+    p.M0 = Fs;
+    p.M1 = Fs;
+    p.mtiles0 = ceil_div(Fs, 128);
+    p.T = T;
+    p.nkb = nkb_d;
+    p.nkb0 = nkb_d;
+    p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
+    p.ldo = 2 * Fs;
+    p.out = h->part;
+    p.err = h->err;
+    LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, st));
+    LMOE_TRY(launch_finalize_glu_bf16(h->part, p.splits, T, Fs, 2 * Fs, h->h_s,
+                                      h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
+                                      h->cfg.situ_linear_beta, st));
+    launches += 2;
+  }
+  // 10 Delta = u_hat W_up^T + h_shared W_shared_down^T
+  {
+    DenseParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a0 = h->m_wup;
+    if (!map_bf16(&p.b0, h->u_hat, din, T, BN)) return LMOE_ERR_CUDA;
+    p.nkb0 = ceil_div(din, 64);
+    p.nkb = p.nkb0;
+    p.mode = 0;
+    if (Fs) {
+      p.mode = 2;
+      p.a1 = h->m_shd;
+      if (!map_bf16(&p.b1, h->h_s, Fs, T, BN)) return LMOE_ERR_CUDA;
+      p.nkb += ceil_div(Fs, 64);
+    }
+    p.M0 = d;
+    p.mtiles0 = ceil_div(d, 128);
+    p.T = T;
+    p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
+    p.ldo = d;
+    p.out = h->part;
+    p.err = h->err;
+    LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+    LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
+    launches += 2;
+  }
+  const size_t n = static_cast<size_t>(T) * h->k;
+  if (topk_idx_opt) LMOE_TRY(cudaMemcpyAsync(topk_idx_opt, h->idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+  if (topk_w_opt) LMOE_TRY(cudaMemcpyAsync(topk_w_opt, h->G, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  h->last_T = T;
+  h->last_launches = launches;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_forward_host(lmoe_handle h, const void* x_host, int T, void* out_host, cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x_host || !out_host) return LMOE_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(T) * h->d * 2;
+  LMOE_TRY(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st));
+  lmoe_status s = lmoe_forward(h, h->x_stage, T, h->out_stage, nullptr, nullptr, st);
+  if (s != LMOE_OK) return s;
+  LMOE_TRY(cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, st));
+  LMOE_TRY(cudaStreamSynchronize(st));
+  return check_err(h);
+}
+
+lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t st) {
+  if (!h || !name || !dst) return LMOE_ERR_INVALID_ARG;
+  const size_t T = static_cast<size_t>(h->last_T);
+  const void* src = nullptr;
+  size_t want = 0;
+  if (!std::strcmp(name, "logits")) {
+    src = h->logits;
+    want = T * h->E * 4;
+  } else if (!std::strcmp(name, "xc")) {
+    src = h->xc;
+    want = T * h->din * 4;
+  } else if (!std::strcmp(name, "u")) {
+    src = h->u;
+    want = T * h->din * 4;
+  } else if (!std::strcmp(name, "u_hat")) {
+    src = h->u_hat;
+    want = T * h->din * 2;
+  } else if (!std::strcmp(name, "h_shared")) {
+    src = h->h_s;
+    want = T * h->Fs * 2;
+  } else if (!std::strcmp(name, "counts")) {
+    src = h->counts;
+    want = static_cast<size_t>(h->E) * 4;
+  } else if (!std::strcmp(name, "offsets")) {
+    src = h->offsets;
+    want = static_cast<size_t>(h->E + 1) * 4;
+  } else if (!std::strcmp(name, "perm")) {
+    src = h->perm;
+    want = T * h->k * 4;
+  } else {
+    return LMOE_ERR_INVALID_ARG;
+  }
+  if (bytes != want) return LMOE_ERR_INVALID_ARG;
+  if (want) LMOE_TRY(cudaMemcpyAsync(dst, src, want, cudaMemcpyDeviceToDevice, st));
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t st) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  LMOE_TRY(cudaStreamSynchronize(st));
+  LMOE_TRY(cudaGetLastError());
+  return check_err(h);
+}
+
+int lmoe_last_launch_count(lmoe_handle h) { return h ? h->last_launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// Internal interfaces between the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace lmoe {
+
+// Error-flag slots in device memory (int[4]): a bounded wait that expired
+// writes kErrTimeout into slot 0; an out-of-range expert index sets slot 1.
+constexpr int kErrTimeout = 1;
+// Largest expert count the dispatch scan handles in one block.
+constexpr int kMaxExperts = 2048;
+
+// ----------------------------------------------------------- dense GEMM
+// out[s][t][row] (fp32 partial sums over split s) = sum_k A[row][k] * B[t][k]
+// for bf16 A (weights, [M][K]) and B (tokens, [T][K]), K-major both.
+//   mode 0: one A, one B.
+//   mode 1: rows [0, M0) from a0, rows [M0, M0+M1) from a1 (M concatenation).
+//   mode 2: k-blocks [0, nkb0) from (a0, b0), the rest from (a1, b1)
+//           (K concatenation, one accumulator).
+struct DenseParams {
+  CUtensorMap a0, a1, b0, b1;
+  float* out;
+  int* err;
+  int mode;
+  int M0, M1, mtiles0;
+  int T;
+  int nkb, nkb0;
+  int splits;
+  int ldo;
+};
+// BN: token tile (32, 64, 128 or 256).  Grid (mtiles, ceil(T/BN), splits).
+cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s);
+
+// Sum `splits` partial planes [splits][T][ld] and apply an epilogue.
+cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,
+                                    cudaStream_t s);
+cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M, int ld, void* out, int ldo,
+                                     const float* add_opt, int ld_add, cudaStream_t s);
+// gate at columns [0, F), up at [F, 2F) of each partial row.
+cudaError_t launch_finalize_glu_bf16(const float* part, int splits, int T, int F, int ld, void* out, int act,
+                                     float b1, float b2, cudaStream_t s);
+
+// ------------------------------------------------------------- routing
+// Also writes the summed logits z [T][E] (fp32) to z_out.
+cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const float* bias, int k,
+                        float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s);
+
+struct DispatchBufs {
+  int32_t* counts;      // [E]
+  int32_t* offsets;     // [E+1]
+  int32_t* perm;        // [T*k]  assignments grouped by expert
+  int32_t* inv_pad;     // [T*k]  padded row of each assignment
+  int32_t* tile_off;    // [E+1]  padded offsets (multiples of BN)
+  int32_t* blockcnt;    // [nchunks][E]
+  int4* tiles;          // [max tiles]  {expert, padded row0, rows, unpadded p0}
+  int32_t* ntiles;      // [1]
+  int* err;
+};
+constexpr int kDispatchChunk = 256;
+cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, const DispatchBufs& b,
+                            cudaStream_t s);
+
+// ------------------------------------------------------- routed experts
+// Activation rows of one assignment: two E4M3 rows (hi, lo) at padded row r
+// (rows 2r, 2r+1 of a [2*Ppad][Kp] byte matrix) and their scales in the
+// tcgen05 staging image, per BN-row tile and 128-wide k-group.
+cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
+                                uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+
+struct MoeGemmParams {
+  CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp]; activations [2*Ppad][Kp]
+  const uint8_t* sfa_gate;       // weight scale atoms [E][MT][G][512]
+  const uint8_t* sfa_up;
+  const uint8_t* sfb;            // activation scale atoms [Ppad/BN][G][NA][512]
+  const int4* tiles;
+  const int32_t* ntiles;
+  const int32_t* perm;
+  const float* G;                // [T*k] routing weights (down pass)
+  int* err;
+  int N_out;                     // output features per expert (F for gate/up, din for down)
+  int MT;                        // ceil(N_out / 128)
+  int KG;                        // Kp / 128
+  // gate/up epilogue: h written as hi/lo E4M3 + scale atoms for the down pass
+  uint8_t* hq;                   // [2*Ppad][Fp]
+  uint8_t* hsf;                  // [Ppad/BN][Fp/128][NA][512]
+  int Fp;
+  int act;
+  float b1, b2;
+  // down epilogue
+  float* y;                      // [T*k][din] fp32, G-scaled expert outputs
+};
+cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+
+// u[t] = sum_j y[t*k + j] (slot order); u_hat = w * u / sqrt(mean(u^2) + eps) -> bf16.
+cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
+                                float* u, void* u_hat, cudaStream_t s);
+
+// Create-time repacking of the expert weights.
+cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MT, int KG, uint8_t* atoms,
+                                cudaStream_t st);
+cudaError_t launch_pad_codes(const uint8_t* q, int E, int N, int K, int Kp, uint8_t* out, cudaStream_t st);
+
+}  // namespace lmoe

@@ -1,0 +1,211 @@
+// Router tail and token -> expert dispatch.
+//
+// topk: per token, sum the router GEMM's split-K partial logits in a fixed
+// order, s = sigmoid(z), c = s + b, select the k largest c (exact ties to the
+// lower expert index), G = scale * s / sum s over the selection (Kimi K3
+// card, router steps; Kimi K2 card adds the 2.827 scale; the selection bias
+// steers the choice only, the weights use the raw sigmoid).
+//
+// dispatch: the counting, argsort and grouping of moe_infer as a stable
+// counting sort that never leaves the device: per-chunk histograms, a scan
+// over chunks and experts, then a per-chunk stable scatter.  It also lays
+// out each expert's assignments in BN-row tiles (segments padded to a
+// multiple of BN) and writes the tile list the grouped expert GEMMs walk.
+#include "common.cuh"
+#include "lmoe_internal.h"
+
+namespace lmoe {
+
+namespace {
+
+constexpr int kTopkWarps = 4;
+
+// One warp per token.  Scores live in shared memory; each selection round
+// every lane finds its best candidate and the warp reduces (value, index).
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ part, int splits, int T,
+                                                               int E, const float* __restrict__ bias, int k,
+                                                               float scale, int32_t* __restrict__ idx,
+                                                               float* __restrict__ G, float* __restrict__ z_out) {
+  extern __shared__ float tk_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= T) return;
+  float* c = tk_smem + static_cast<size_t>(warp) * 2 * E;
+  float* sg = c + E;
+  const size_t plane = static_cast<size_t>(T) * E;
+  for (int e = lane; e < E; e += 32) {
+    float z = 0.f;
+    for (int s = 0; s < splits; ++s) z += part[s * plane + static_cast<size_t>(t) * E + e];
+    z_out[static_cast<size_t>(t) * E + e] = z;
+    const float sv = sigmoidf_(z);
+    sg[e] = sv;
+    c[e] = sv + bias[e];
+  }
+  __syncwarp();
+  float sel_s[32];
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int e = lane; e < E; e += 32) {
+      const float v = c[e];
+      if (v > bv) {  // e increases along the lane's scan: ties keep the lower index
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < 0 || bi >= E) bi = 0;  // only if every score were NaN
+    sel_s[j] = sg[bi];
+    if (lane == 0) {
+      idx[static_cast<size_t>(t) * k + j] = bi;
+      c[bi] = -INFINITY;
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += sel_s[j];
+    const float inv = scale / sum;
+    for (int j = 0; j < k; ++j) G[static_cast<size_t>(t) * k + j] = sel_s[j] * inv;
+  }
+}
+
+// Per-chunk histogram of expert ids.
+__global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int P, int E, int32_t* __restrict__ blockcnt,
+                                      int* err) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int a0 = blockIdx.x * kDispatchChunk;
+  for (int a = a0 + threadIdx.x; a < min(P, a0 + kDispatchChunk); a += blockDim.x) {
+    const int e = idx[a];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else if (err) atomicExch(err + 1, 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One block: per-expert prefix over chunks, exclusive scans over experts
+// (plain and BN-padded), the tile list.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ blockcnt, int nchunks, int E,
+                                                             int BN, int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets,
+                                                             int32_t* __restrict__ tile_off, int4* __restrict__ tiles,
+                                                             int32_t* __restrict__ ntiles) {
+  __shared__ int32_t s_cnt[kMaxExperts];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  __shared__ int32_t s_toff[kMaxExperts + 1];
+  __shared__ int32_t s_tiles[kMaxExperts + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nchunks; ++b) {
+      const int c = blockcnt[static_cast<size_t>(b) * E + e];
+      blockcnt[static_cast<size_t>(b) * E + e] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, to = 0, nt = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = o;
+      s_toff[e] = to;
+      s_tiles[e] = nt;
+      const int c = s_cnt[e];
+      const int n = (c + BN - 1) / BN;
+      o += c;
+      to += n * BN;
+      nt += n;
+    }
+    s_off[E] = o;
+    s_toff[E] = to;
+    s_tiles[E] = nt;
+    *ntiles = nt;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    offsets[e] = s_off[e];
+    tile_off[e] = s_toff[e];
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int base = s_off[e];
+    for (int b = 0; b < nchunks; ++b) blockcnt[static_cast<size_t>(b) * E + e] += base;
+    const int c = s_cnt[e];
+    for (int i = 0, ti = s_tiles[e]; i * BN < c; ++i, ++ti)
+      tiles[ti] = make_int4(e, s_toff[e] + i * BN, min(BN, c - i * BN), base + i * BN);
+  }
+}
+
+// One warp per chunk: stable ranks inside the chunk, in assignment order.
+__global__ void __launch_bounds__(32) dispatch_scatter_kernel(const int32_t* __restrict__ idx, int P, int E,
+                                                              const int32_t* __restrict__ blockcnt,
+                                                              const int32_t* __restrict__ offsets,
+                                                              const int32_t* __restrict__ tile_off,
+                                                              int32_t* __restrict__ perm,
+                                                              int32_t* __restrict__ inv_pad) {
+  extern __shared__ int32_t pos[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) pos[e] = blockcnt[static_cast<size_t>(blockIdx.x) * E + e];
+  __syncwarp();
+  const int a0 = blockIdx.x * kDispatchChunk;
+  for (int s = 0; s < kDispatchChunk; s += 32) {
+    const int a = a0 + s + lane;
+    const bool valid = a < P;
+    int e = valid ? idx[a] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int base = e >= 0 ? pos[e] : 0;
+    __syncwarp();
+    if (e >= 0) {
+      const int p = base + rank;
+      perm[p] = a;
+      inv_pad[a] = tile_off[e] + (p - offsets[e]);
+      if (rank == 0) pos[e] = base + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const float* bias, int k,
+                        float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
+  const size_t smem = static_cast<size_t>(kTopkWarps) * 2 * E * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logit_part, splits, T, E, bias, k, routed_scale, idx, G,
+                                                     z_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, const DispatchBufs& b,
+                            cudaStream_t s) {
+  const int P = T * k;
+  if (P <= 0) return cudaSuccess;
+  const int nchunks = (P + kDispatchChunk - 1) / kDispatchChunk;
+  const size_t hsmem = static_cast<size_t>(E) * sizeof(int32_t);
+  dispatch_count_kernel<<<nchunks, 256, hsmem, s>>>(idx, P, E, b.blockcnt, b.err);
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.blockcnt, nchunks, E, BN, b.counts, b.offsets, b.tile_off, b.tiles,
+                                          b.ntiles);
+  dispatch_scatter_kernel<<<nchunks, 32, hsmem, s>>>(idx, P, E, b.blockcnt, b.offsets, b.tile_off, b.perm,
+                                                     b.inv_pad);
+  return cudaGetLastError();
+}
+
+}  // namespace lmoe
