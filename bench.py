@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""Benchmark of the Stable LatentMoE layer forward on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one lmoe_forward of the whole layer (router, dispatch, latent
+down-projection, routed MXFP4 experts, combine + RMSNorm, shared experts,
+output GEMM) over one batch of seeded synthetic tokens; weights and tokens
+resident in HBM.  Tokens rotate over 4 seeded batches so the routed expert
+set changes between steps; every step streams the selected experts' weights
+(~11 GB at T = 64), far more than the 129 MB L2, so no flush is needed.
+
+Under torchrun (N > 1) every rank runs its own replica on its own tokens
+(the layer is per-token: no collective on the data path); value = tokens of
+all ranks / the slowest rank's time.
+
+Prints one JSON line: metric/value (device-timed tokens/s), e2e (through
+lmoe_forward_host with host buffers and the copies inside the timed
+region), roofline of the dominant kernel (the grouped MXFP4 gate/up GEMM,
+algorithmic bytes over its CUDA-event time), the whole-layer HBM roofline,
+per-stage times, clocks sampled during the timed region, and the fp64
+oracle timed on the host cores as cpu_baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
+UNIT = "tokens/s"
+EXPERT_BYTES = 17_547_264          # one K3 expert: 3 x 3584 x 3072 E2M1 codes + E8M0 scales
+DENSE_BYTES = 379_857_408          # K3 bf16 router, W_down, W_up, norm, shared MLP + fp32 bias
+TOKEN_IO_BYTES = 28_672            # x in + Delta out, bf16, per token
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"], src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        # one GPU per box: sample every visible GPU
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        """Samples taken between host times t0 and t1 (the timed region)."""
+        import datetime
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = [[c.strip() for c in r.split(",")] for r in open(self.f.name).read().strip().splitlines()
+                if r.count(",") >= 9]
+        os.unlink(self.f.name)
+
+        def ts(r):
+            try:
+                return datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in rows if ts(r) is not None and t0 <= ts(r) <= t1]
+        rows = inside if inside else rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        pw = [num(r[4]) for r in rows if num(r[4]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------- cpu oracle
+def oracle_for(wl, W_dev):
+    import oracle as O
+    dense = {k: v for k, v in W_dev.items() if not k.startswith("ex_")}
+    Wn = O.numpy_inputs(dense)
+    Wn["expert_fn"] = lambda name, e: (W_dev[name + "_q"][e].cpu().numpy(), W_dev[name + "_s"][e].cpu().numpy())
+    return O, Wn
+
+
+def cpu_baseline(wl, W_dev, x_dev, ntok=2) -> dict:
+    """The fp64 oracle, as it stands, on the first `ntok` tokens of a batch
+    (its routing, 16 fresh expert dequantisations per token, dense parts)."""
+    import numpy as np
+    import torch
+    O, Wn = oracle_for(wl, W_dev)
+    xb = x_dev[:ntok].cpu().view(torch.int16).numpy().view(np.uint16)
+    layer = O.Layer(wl.cfg, Wn)
+    for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w", "sh_gate", "sh_up", "sh_down"):
+        layer.dense(name)            # host-side fp64 copies of the dense weights: input preparation
+    t0 = time.perf_counter()
+    O.forward(layer, xb)
+    dt = time.perf_counter() - t0
+    return {"value": ntok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{ntok} tokens of the {wl.name} batch through the fp64 oracle (routing, "
+                      f"{ntok * wl.cfg.top_k} expert dequantisations, dense parts); numpy BLAS threads = default",
+            "seconds": dt}
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from lmoe_inputs import configs as C
+    from lmoe_inputs import generate as G
+    from latent_mixture_experts_gb300 import LatentMoE, build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    wl = C.workload(args.workload)
+    T, cfg = wl.T, wl.cfg
+    W = G.gen_weights(wl, device="cuda")
+    xs = [G.gen_x(replace(wl, seed=wl.seed + 7919 * (rank * 8 + i + 1)), device="cuda") for i in range(4)]
+    out = torch.empty(T, cfg.d_model, dtype=torch.bfloat16, device="cuda")
+    layer = LatentMoE(cfg, W, max_tokens=T)
+    stream = torch.cuda.current_stream()
+
+    # distinct experts each batch selects (units of the expert bytes)
+    U = []
+    for xb in xs:
+        layer.lmoe_forward(xb, out=out)
+        U.append(layer.lmoe_last_active_experts())
+    layer.lmoe_sync_status()
+    launches = layer.lmoe_last_launch_count()
+
+    for i in range(args.warmup):
+        layer.lmoe_forward(xs[i % 4], out=out)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    layer.lmoe_set_profiling(args.steps)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    clk = ClockSampler(uuid)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        layer.lmoe_forward(xs[i % 4], out=out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop(t_start, t_end)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    prof = layer.lmoe_profile_get()
+    layer.lmoe_set_profiling(0)
+    layer.lmoe_sync_status()
+
+    steps = args.steps
+    ms_step = ms / steps
+    value = world * T * steps / (ms / 1e3)
+    U_mean = sum(U[i % 4] for i in range(steps)) / steps
+    pk = peaks()
+
+    # dominant kernel: grouped MXFP4 gate/up GEMM.  Algorithmic bytes per
+    # launch: the selected experts' gate+up codes and scales, the hi/lo E4M3
+    # activations in (with their scales) and the hi/lo h out.
+    din, F, k = cfg.d_latent, cfg.d_expert_ff, cfg.top_k
+    gu_w = 2 * (F * din // 2 + F * din // 32)
+    gu_bytes = U_mean * gu_w + T * k * (2 * din + 2 * din // 32) + T * k * (2 * F + 2 * F // 32)
+    gu_ms, gu_n = prof["expert_gate_up"]
+    gu_avg = gu_ms / max(gu_n, 1)
+    achieved = gu_bytes / (gu_avg * 1e-3) / 1e9
+    dn_w = din * F // 2 + din * F // 32
+    dn_bytes = U_mean * dn_w + T * k * (2 * F + 2 * F // 32) + T * k * din * 4
+    dn_ms, dn_n = prof["expert_down"]
+    layer_bytes = DENSE_BYTES + U_mean * EXPERT_BYTES + T * TOKEN_IO_BYTES
+    stages = {name: round(v[0] / max(v[1], 1), 5) for name, v in prof.items()}
+
+    # end to end through the host-buffer entry point
+    xh = [xb.cpu().pin_memory() for xb in xs]
+    oh = torch.empty(T, cfg.d_model, dtype=torch.bfloat16).pin_memory()
+    for i in range(2):
+        layer.lmoe_forward_host(xh[i], oh)
+    n_e2e = max(10, min(steps, 200))
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        layer.lmoe_forward_host(xh[i % 4], oh)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * T * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * cfg.d_model * 2,
+           "d2h_bytes_per_step": T * cfg.d_model * 2, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, W, xs[0], ntok=args.cpu_tokens)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1 x e4m3(hi+lo) block-scaled; bf16 dense; fp32 accumulate",
+        "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to MXFP4; x ~ N(0,1) bf16)",
+        "config": {"workload": wl.name, "T": T, "d_model": cfg.d_model, "d_latent": din, "n_experts": cfg.n_experts,
+                   "top_k": k, "d_expert_ff": F, "d_shared_ff": cfg.d_shared_ff, "expert_format": cfg.expert_wfmt,
+                   "parallelism": f"replicas x{world}", "token_batches_rotated": 4,
+                   "l2": "no flush: each step streams the selected experts' weights (GBs) >> 129 MB L2",
+                   "active_experts_mean": round(U_mean, 1)},
+        "roofline": {"kernel": "moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_avg, 5),
+                     "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"},
+        "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),
+                           "achieved": round(layer_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": pk["hbm"],
+                           "unit": "GB/s", "frac": round(layer_bytes / (ms_step * 1e-3) / 1e9 / pk["hbm"], 4)},
+        "down_kernel": {"achieved": round(dn_bytes / (dn_ms / max(dn_n, 1) * 1e-3) / 1e9, 1), "unit": "GB/s",
+                        "ms_per_launch": round(dn_ms / max(dn_n, 1), 5)},
+        "stage_ms": stages,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches * steps,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- reference
+def run_reference(args):
+    """The fp64 oracle as the reference arm, on the host cores.  One step is
+    one (token, slot) assignment: the step at slot 0 also runs the token's
+    router, latent down-projection and shared MLP, the step at the last slot
+    its RMSNorm and up-projection; every step dequantises and applies one
+    routed expert afresh.  k steps = one token."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from lmoe_inputs import configs as C
+    from lmoe_inputs import generate as G
+    import oracle as O
+
+    wl = C.workload(args.workload)
+    cfg = wl.cfg
+    k = cfg.top_k
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ntok = (args.warmup + args.steps + k - 1) // k + 1
+    x = G.gen_x(replace(wl, seed=wl.seed + 7919), device="cpu", T=max(ntok, 1))
+    W_dense = {}
+    for name, shape, fan in (("router_w", (cfg.n_experts, cfg.d_model), cfg.d_model),
+                             ("w_down_latent", (cfg.d_latent, cfg.d_model), cfg.d_model),
+                             ("w_up_latent", (cfg.d_model, cfg.d_latent), cfg.d_latent),
+                             ("sh_gate", (cfg.d_shared_ff, cfg.d_model), cfg.d_model),
+                             ("sh_up", (cfg.d_shared_ff, cfg.d_model), cfg.d_model),
+                             ("sh_down", (cfg.d_model, cfg.d_shared_ff), cfg.d_shared_ff)):
+        W_dense[name] = G.gen_dense(wl, name, shape, fan, device=dev).cpu()
+    W_dense["router_bias"] = G.gen_router_bias(wl)
+    W_dense["norm_w"] = G.to_bf16(1.0 + G.normal_f32(cfg.d_latent, G.stream_key(wl.seed, G.TAG["norm_w"]), "cpu",
+                                                     0.02))
+    Wn = O.numpy_inputs(W_dense)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    layer = O.Layer(cfg, Wn)
+    for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w", "sh_gate", "sh_up", "sh_down"):
+        layer.dense(name)
+    xo = O.bf16_bits_to_f64(xb)
+    routes = O.router(xo, layer.dense("router_w"), Wn["router_bias"], k, cfg.routed_scale)
+    # expert codes of every assignment the run touches (input preparation, untimed)
+    total = args.warmup + args.steps
+    need = {}
+    for s in range(total):
+        t, j = divmod(s, k)
+        e = int(routes["idx"][t, j])
+        for m in ("ex_gate", "ex_up", "ex_down"):
+            if (m, e) not in need:
+                q, sc = G.gen_expert(wl, m, e, device=dev)
+                need[(m, e)] = (q.cpu().numpy(), sc.cpu().numpy())
+
+    state = {}
+
+    def step(s):
+        t, j = divmod(s, k)
+        if j == 0:
+            state["xc"] = xo[t] @ layer.dense("w_down_latent").T
+            state["u"] = np.zeros(cfg.d_latent)
+            g = xo[t] @ layer.dense("sh_gate").T
+            u = xo[t] @ layer.dense("sh_up").T
+            state["ys"] = layer.act(g, u) @ layer.dense("sh_down").T
+        e = int(routes["idx"][t, j])
+        Wg = O.dequant_mxfp4(*need[("ex_gate", e)])
+        Wu = O.dequant_mxfp4(*need[("ex_up", e)])
+        Wd = O.dequant_mxfp4(*need[("ex_down", e)])
+        h = layer.act(Wg @ state["xc"], Wu @ state["xc"])
+        state["u"] += routes["G"][t, j] * (Wd @ h)
+        if j == k - 1:
+            uh = O.rms_norm(state["u"], layer.dense("norm_w"), cfg.norm_eps)
+            state["delta"] = uh @ layer.dense("w_up_latent").T + state["ys"]
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.warmup, total):
+        step(s)
+    dt = time.perf_counter() - t0
+    value = (args.steps / k) / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded generator)",
+        "config": {"workload": wl.name, "T": wl.T, "d_model": cfg.d_model, "d_latent": cfg.d_latent,
+                   "n_experts": cfg.n_experts, "top_k": k},
+        "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": round(value, 4), "unit": UNIT,
+                         "sample": f"{args.steps} (token, slot) assignments = {args.steps / k:.2f} tokens "
+                                   f"of {wl.name}; each step dequantises and applies one routed expert, "
+                                   "slot 0 / last slot add the token's dense parts"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="k3_decode_t64")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -168,6 +168,30 @@ LMOE_API lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t stream);
 /* Number of kernels the last lmoe_forward launched (for launch accounting). */
 LMOE_API int lmoe_last_launch_count(lmoe_handle h);
 
+/* Per-stage timing.  While enabled, lmoe_forward records a CUDA event pair
+ * on its stream around each stage below; lmoe_profile_get synchronises the
+ * recorded events and returns the stage's summed device time (ms) and the
+ * number of timed launches since profiling was last enabled.  Enabling
+ * again resets the sums.  Stages: */
+enum {
+  LMOE_STAGE_ROUTER = 0,     /* router GEMM + top-k */
+  LMOE_STAGE_DISPATCH = 1,   /* counting-sort dispatch */
+  LMOE_STAGE_LATENT_DOWN = 2,/* x^c GEMM (+ split-K sum) */
+  LMOE_STAGE_ACT_QUANT = 3,  /* x^c -> hi/lo E4M3 in expert-tile order */
+  LMOE_STAGE_EXPERT_GU = 4,  /* grouped MXFP4 gate/up GEMM + SiTU */
+  LMOE_STAGE_EXPERT_DOWN = 5,/* grouped MXFP4 down GEMM x G */
+  LMOE_STAGE_COMBINE = 6,    /* slot-ordered sum + RMSNorm */
+  LMOE_STAGE_SHARED = 7,     /* shared gate/up GEMM + SiTU */
+  LMOE_STAGE_OUTPUT = 8,     /* [u_hat | h_shared] output GEMM */
+  LMOE_NUM_STAGES = 9
+};
+LMOE_API lmoe_status lmoe_set_profiling(lmoe_handle h, int enable);
+LMOE_API lmoe_status lmoe_profile_get(lmoe_handle h, int stage, float* total_ms, int* count);
+
+/* Number of distinct experts the last lmoe_forward's batch selected
+ * (synchronises the stream; reads the dispatch counts). */
+LMOE_API int lmoe_last_active_experts(lmoe_handle h, cudaStream_t stream);
+
 /* Release the workspace.  Synchronises the device work of this handle.
  * NULL is accepted. */
 LMOE_API lmoe_status lmoe_destroy(lmoe_handle h);

@@ -21,8 +21,10 @@ LMOE_W_MXFP4, LMOE_W_FP8_BLOCK128 = 0, 1
 
 # Every symbol include/lmoe.h declares.
 EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lmoe_dispatch",
-           "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_destroy",
-           "lmoe_status_string")
+           "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_set_profiling",
+           "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string")
+STAGES = ("router", "dispatch", "latent_down", "act_quant", "expert_gate_up", "expert_down", "combine_norm",
+          "shared", "output")
 
 
 class LmoeConfig(ctypes.Structure):
@@ -70,6 +72,9 @@ def load_library(path: str = LIB_PATH):
             "lmoe_debug_tensor": (I, [P, ctypes.c_char_p, P, S, P]),
             "lmoe_sync_status": (I, [P, P]),
             "lmoe_last_launch_count": (I, [P]),
+            "lmoe_set_profiling": (I, [P, I]),
+            "lmoe_profile_get": (I, [P, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
+            "lmoe_last_active_experts": (I, [P, P]),
             "lmoe_destroy": (I, [P]),
             "lmoe_status_string": (ctypes.c_char_p, [I]),
         }
@@ -192,6 +197,21 @@ class LatentMoE:
 
     def lmoe_last_launch_count(self) -> int:
         return int(self._lib.lmoe_last_launch_count(self._h))
+
+    def lmoe_set_profiling(self, reserve_forwards: int):
+        _check("lmoe_set_profiling", self._lib.lmoe_set_profiling(self._h, int(reserve_forwards)))
+
+    def lmoe_profile_get(self) -> dict:
+        """{stage name: (summed ms, launches)} since profiling was enabled."""
+        out = {}
+        for i, name in enumerate(STAGES):
+            ms, n = ctypes.c_float(), ctypes.c_int()
+            _check("lmoe_profile_get", self._lib.lmoe_profile_get(self._h, i, ctypes.byref(ms), ctypes.byref(n)))
+            out[name] = (ms.value, n.value)
+        return out
+
+    def lmoe_last_active_experts(self, stream=None) -> int:
+        return int(self._lib.lmoe_last_active_experts(self._h, _stream(stream)))
 
     def lmoe_destroy(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -56,6 +56,10 @@ struct lmoe_ctx {
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd, m_exg, m_exu, m_exd;
   int last_T = 0;
   int last_launches = 0;
+  // per-stage event timing
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_free;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_used[LMOE_NUM_STAGES];
 };
 
 namespace {
@@ -124,6 +128,49 @@ long long max_split_rows(int mtiles, int nkb, int Tm, int num_sms) {
   return best;
 }
 
+cudaEvent_t take_event(lmoe_ctx* h) {
+  if (!h->ev_free.empty()) {
+    cudaEvent_t e = h->ev_free.back();
+    h->ev_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Records a CUDA event pair around one stage's launches while profiling.
+struct StageTimer {
+  lmoe_ctx* h;
+  int stage;
+  cudaStream_t st;
+  cudaEvent_t b = nullptr;
+  StageTimer(lmoe_ctx* h_, int stage_, cudaStream_t st_) : h(h_), stage(stage_), st(st_) {
+    if (h->prof && (b = take_event(h)) != nullptr) cudaEventRecord(b, st);
+  }
+  void done() {
+    if (!b) return;
+    cudaEvent_t e = take_event(h);
+    if (e) {
+      cudaEventRecord(e, st);
+      h->ev_used[stage].emplace_back(b, e);
+    } else {
+      h->ev_free.push_back(b);
+    }
+    b = nullptr;
+  }
+};
+
+void release_events(lmoe_ctx* h) {
+  for (auto& v : h->ev_used) {
+    for (auto& pr : v) {
+      h->ev_free.push_back(pr.first);
+      h->ev_free.push_back(pr.second);
+    }
+    v.clear();
+  }
+}
+
 lmoe_status check_err(lmoe_ctx* h) {
   int e[4] = {0, 0, 0, 0};
   LMOE_TRY(cudaMemcpy(e, h->err, sizeof(e), cudaMemcpyDeviceToHost));
@@ -134,6 +181,7 @@ lmoe_status check_err(lmoe_ctx* h) {
 }
 
 lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& launches) {
+  StageTimer tm(h, LMOE_STAGE_ROUTER, st);
   const int BN = dense_bn(T);
   DenseParams p;
   std::memset(&p, 0, sizeof(p));
@@ -153,11 +201,13 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
   LMOE_TRY(launch_topk(h->part, p.splits, T, h->E, h->w.router_bias, h->k, h->cfg.routed_scale, h->idx, h->G,
                        h->logits, st));
   launches += 2;
+  tm.done();
   return LMOE_OK;
 }
 
 lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t* counts, int32_t* offsets,
                          int32_t* perm, cudaStream_t st, int& launches) {
+  StageTimer tm(h, LMOE_STAGE_DISPATCH, st);
   DispatchBufs b;
   b.counts = counts;
   b.offsets = offsets;
@@ -170,6 +220,7 @@ lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t
   b.err = h->err;
   LMOE_TRY(launch_dispatch(idx, T, h->k, h->E, BN, b, st));
   launches += 3;
+  tm.done();
   return LMOE_OK;
 }
 
@@ -371,6 +422,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
 lmoe_status lmoe_destroy(lmoe_handle h) {
   if (!h) return LMOE_OK;
   cudaError_t e = cudaDeviceSynchronize();
+  release_events(h);
+  for (cudaEvent_t ev : h->ev_free) cudaEventDestroy(ev);
   cudaFree(h->pool);
   delete h;
   return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
@@ -419,6 +472,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
 
   // 4 latent down-projection
   {
+    StageTimer tm(h, LMOE_STAGE_LATENT_DOWN, st);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_wdown;
@@ -439,10 +493,15 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
       LMOE_TRY(launch_finalize_sum_f32(h->part, p.splits, T, din, din, h->xc, din, st));
       ++launches;
     }
+    tm.done();
   }
   // 5 activations -> hi/lo E4M3 in expert-tile order
-  LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
-  ++launches;
+  {
+    StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
+    LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+    ++launches;
+    tm.done();
+  }
   // 6-7 routed experts
   {
     MoeGemmParams p;
@@ -468,8 +527,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.b1 = h->cfg.situ_beta;
     p.b2 = h->cfg.situ_linear_beta;
     p.y = h->y;
+    StageTimer tgu(h, LMOE_STAGE_EXPERT_GU, st);
     LMOE_TRY(launch_moe_gate_up(p, BNm, h->num_sms, st));
     ++launches;
+    tgu.done();
     MoeGemmParams q = p;
     q.a_gate = h->m_exd;
     if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
@@ -479,15 +540,22 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.N_out = din;
     q.MT = h->MT_dn;
     q.KG = h->KG_dn;
+    StageTimer tdn(h, LMOE_STAGE_EXPERT_DOWN, st);
     LMOE_TRY(launch_moe_down(q, BNm, h->num_sms, st));
     ++launches;
+    tdn.done();
   }
   // 8 expert sum in slot order + latent RMSNorm
-  LMOE_TRY(launch_combine_norm(h->y, T, h->k, din, h->w.norm_w, h->cfg.use_latent_norm, h->cfg.norm_eps, h->u,
-                               h->u_hat, st));
-  ++launches;
+  {
+    StageTimer tm(h, LMOE_STAGE_COMBINE, st);
+    LMOE_TRY(launch_combine_norm(h->y, T, h->k, din, h->w.norm_w, h->cfg.use_latent_norm, h->cfg.norm_eps, h->u,
+                                 h->u_hat, st));
+    ++launches;
+    tm.done();
+  }
   // 9 shared experts gate/up + SiTU
   if (Fs) {
+    StageTimer tm(h, LMOE_STAGE_SHARED, st);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_shg;
@@ -509,9 +577,11 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
                                       h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
                                       h->cfg.situ_linear_beta, st));
     launches += 2;
+    tm.done();
   }
   // 10 Delta = u_hat W_up^T + h_shared W_shared_down^T
   {
+    StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_wup;
@@ -535,6 +605,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
     LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
     launches += 2;
+    tm.done();
   }
   const size_t n = static_cast<size_t>(T) * h->k;
   if (topk_idx_opt) LMOE_TRY(cudaMemcpyAsync(topk_idx_opt, h->idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
@@ -602,5 +673,44 @@ lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t st) {
 }
 
 int lmoe_last_launch_count(lmoe_handle h) { return h ? h->last_launches : 0; }
+
+lmoe_status lmoe_set_profiling(lmoe_handle h, int enable) {
+  if (!h || enable < 0) return LMOE_ERR_INVALID_ARG;
+  release_events(h);
+  h->prof = enable > 0;
+  // enable > 0 also reserves event pairs for that many forwards
+  const size_t want = static_cast<size_t>(enable) * 2 * LMOE_NUM_STAGES;
+  while (h->prof && h->ev_free.size() < want) {
+    cudaEvent_t e = nullptr;
+    LMOE_TRY(cudaEventCreate(&e));
+    h->ev_free.push_back(e);
+  }
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_profile_get(lmoe_handle h, int stage, float* total_ms, int* count) {
+  if (!h || stage < 0 || stage >= LMOE_NUM_STAGES || !total_ms || !count) return LMOE_ERR_INVALID_ARG;
+  double sum = 0.0;
+  for (auto& pr : h->ev_used[stage]) {
+    LMOE_TRY(cudaEventSynchronize(pr.second));
+    float ms = 0.f;
+    LMOE_TRY(cudaEventElapsedTime(&ms, pr.first, pr.second));
+    sum += ms;
+  }
+  *total_ms = static_cast<float>(sum);
+  *count = static_cast<int>(h->ev_used[stage].size());
+  return LMOE_OK;
+}
+
+int lmoe_last_active_experts(lmoe_handle h, cudaStream_t st) {
+  if (!h || h->last_T <= 0) return 0;
+  std::vector<int32_t> c(h->E);
+  if (cudaMemcpyAsync(c.data(), h->counts, c.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  int n = 0;
+  for (int32_t v : c) n += v > 0;
+  return n;
+}
 
 }  // extern "C"

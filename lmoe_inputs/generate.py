@@ -199,6 +199,32 @@ def gen_expert(wl: Workload, name: str, e: int, device="cpu"):
     return quantise_fp8_block128(w)
 
 
+def gen_experts_mxfp4(wl: Workload, name: str, device, chunk: int = 16):
+    """All experts of one MXFP4 matrix, `chunk` experts per batch of tensor
+    ops: the same bytes as gen_expert one expert at a time (each expert keeps
+    its own stream key), with far fewer kernel launches on a GPU."""
+    cfg = wl.cfg
+    din, F, E = cfg.d_expert_in, cfg.d_expert_ff, cfg.n_experts
+    N, K = (F, din) if name in ("ex_gate", "ex_up") else (din, F)
+    q_all = torch.empty((E, N, K // 2), dtype=torch.uint8, device=device)
+    s_all = torch.empty((E, N, K // 32), dtype=torch.uint8, device=device)
+    std = torch.tensor(_std(K), dtype=torch.float32, device=device)
+    idx = torch.arange(N * K, dtype=torch.int64, device=device)
+    table = _norm_table(device)
+    for e0 in range(0, E, chunk):
+        es = range(e0, min(E, e0 + chunk))
+        keys = [stream_key(wl.seed, TAG[name], e) for e in es]
+        k1 = torch.tensor(keys, dtype=torch.int64, device=device)[:, None]
+        k2 = torch.tensor([_hash32_int(k ^ 0x27D4EB2F) for k in keys], dtype=torch.int64, device=device)[:, None]
+        h = hash32(hash32(idx[None, :] ^ k1) ^ k2)
+        w = (table[h & ((1 << _TABLE_BITS) - 1)] * std).view(len(es) * N, K)
+        q, s = quantise_mxfp4(w)
+        q_all[e0:e0 + len(es)] = q.view(len(es), N, K // 2)
+        s_all[e0:e0 + len(es)] = s.view(len(es), N, K // 32)
+        del h, w, q, s
+    return q_all, s_all
+
+
 def gen_shared_fp8(wl: Workload, name: str, device="cpu"):
     cfg = wl.cfg
     d, Fs = cfg.d_model, cfg.d_shared_ff
@@ -221,6 +247,9 @@ def gen_weights(wl: Workload, device="cpu") -> dict:
             nw = 1.0 + normal_f32(l, stream_key(wl.seed, TAG["norm_w"]), "cpu", 0.02)
             W["norm_w"] = to_bf16(nw).to(device)
     for name in ("ex_gate", "ex_up", "ex_down"):
+        if device != "cpu" and cfg.expert_wfmt == "mxfp4":
+            W[name + "_q"], W[name + "_s"] = gen_experts_mxfp4(wl, name, device)
+            continue
         for e in range(E):
             q, s = gen_expert(wl, name, e, device)
             if e == 0:

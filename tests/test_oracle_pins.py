@@ -405,3 +405,14 @@ def test_k2_routed_scale_is_linear():
         u = layer.expert("ex_up", e) @ xt
         acc = acc + a["routes"]["G"][0, j] * (layer.expert("ex_down", e) @ (g / (1 + np.exp(-g)) * u))
     assert np.allclose(acc, a["y_routed"][0], rtol=1e-12, atol=1e-12)
+
+
+def test_batched_expert_generation_matches_per_expert():
+    """The batched generator (used on GPUs) yields the bytes of the
+    one-expert-at-a-time generator the oracle's inputs come from."""
+    wl = C.workload("k3_tiny_t16")
+    for name in ("ex_gate", "ex_down"):
+        qa, sa = G.gen_experts_mxfp4(wl, name, "cpu", chunk=5)
+        for e in (0, 7, 63):
+            q, s = G.gen_expert(wl, name, e)
+            assert torch.equal(qa[e], q) and torch.equal(sa[e], s)
