@@ -153,6 +153,31 @@ LMOE_API lmoe_status lmoe_forward_host(lmoe_handle h, const void* x_host, int T,
 LMOE_API lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t* counts, int32_t* offsets,
                           int32_t* perm, cudaStream_t stream);
 
+/* lmoe_dispatch for callers that cannot allocate device memory.  The paper
+ * has no counterpart of this call: it exists for code that may not call
+ * cudaMalloc (and therefore cannot lmoe_create a handle), such as a step
+ * being recorded into a CUDA graph that must not allocate, a plug-in whose
+ * host framework owns the whole device-memory budget, or an allocator-free
+ * runtime.  Same inputs and outputs as lmoe_dispatch (topk_idx int32
+ * [T][k] in; counts [E], offsets [E+1], perm [T*k] out, all device memory
+ * the caller provides) plus k and n_experts, since there is no handle.
+ * Scratch: one static device array of about 2.4 MiB inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Limits: T*k <= LMOE_NOALLOC_MAX_ASSIGNMENTS, n_experts <=
+ * LMOE_NOALLOC_MAX_EXPERTS; larger sizes return LMOE_ERR_INVALID_ARG before
+ * anything is launched.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it: make that first call
+ * outside any stream capture.  All calls share the one array, so calls that
+ * overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller; no part of the array needs to start at zero
+ * (every word a call reads is written earlier in the same call).  Expert ids
+ * outside [0, n_experts) are skipped without an error report. */
+#define LMOE_NOALLOC_MAX_ASSIGNMENTS 65536
+#define LMOE_NOALLOC_MAX_EXPERTS 2048
+LMOE_API lmoe_status lmoe_dispatch_noalloc(const int32_t* topk_idx, int T, int k, int n_experts, int32_t* counts,
+                                           int32_t* offsets, int32_t* perm, cudaStream_t stream);
+
 /* Copy an intermediate of the last lmoe_forward on this handle out of the
  * workspace (stream-ordered): "logits" fp32 [T][E] (router z), "xc" fp32
  * [T][l], "u" fp32 [T][l] (expert sum), "u_hat" bf16 [T][l], "h_shared"

@@ -22,7 +22,10 @@ LMOE_W_MXFP4, LMOE_W_FP8_BLOCK128 = 0, 1
 # Every symbol include/lmoe.h declares.
 EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lmoe_dispatch",
            "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_set_profiling",
-           "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string")
+           "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string",
+           "lmoe_dispatch_noalloc")
+NOALLOC_MAX_ASSIGNMENTS = 65536
+NOALLOC_MAX_EXPERTS = 2048
 STAGES = ("router", "dispatch", "latent_down", "act_quant", "expert_gate_up", "expert_down", "combine_norm",
           "shared", "output")
 
@@ -77,6 +80,7 @@ def load_library(path: str = LIB_PATH):
             "lmoe_last_active_experts": (I, [P, P]),
             "lmoe_destroy": (I, [P]),
             "lmoe_status_string": (ctypes.c_char_p, [I]),
+            "lmoe_dispatch_noalloc": (I, [P, I, I, I, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -104,6 +108,17 @@ def _stream(stream):
 def _check(call: str, st: int):
     if st != LMOE_OK:
         raise LmoeError(call, st)
+
+
+def lmoe_dispatch_noalloc(topk_idx: torch.Tensor, n_experts: int, counts: torch.Tensor, offsets: torch.Tensor,
+                          perm: torch.Tensor, stream=None) -> None:
+    """Handle-free dispatch for callers that cannot allocate device memory:
+    the caller passes every output buffer (counts int32 [E], offsets int32
+    [E+1], perm int32 [T*k]); the library's scratch is a static device array
+    (T*k <= 65536, E <= 2048).  Calls that overlap on the GPU race."""
+    T, k = topk_idx.shape
+    _check("lmoe_dispatch_noalloc", load_library().lmoe_dispatch_noalloc(
+        _ptr(topk_idx), T, k, int(n_experts), _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)))
 
 
 def make_config(cfg, max_tokens: int) -> LmoeConfig:
