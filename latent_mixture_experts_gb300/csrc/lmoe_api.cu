@@ -219,7 +219,7 @@ lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t
   b.ntiles = h->ntiles;
   b.err = h->err;
   LMOE_TRY(launch_dispatch(idx, T, h->k, h->E, BN, b, st));
-  launches += 3;
+  launches += dispatch_launches(T * h->k);
   tm.done();
   return LMOE_OK;
 }
@@ -519,6 +519,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.err = h->err;
     p.N_out = h->F;
     p.MT = h->MT_gu;
+    p.MTa = h->MT_gu;
     p.KG = h->KG_gu;
     p.hq = h->hq;
     p.hsf = h->hsf;
@@ -538,7 +539,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
     q.N_out = din;
-    q.MT = h->MT_dn;
+    q.MT = (h->MT_dn + 1) / 2;
+    q.MTa = h->MT_dn;
     q.KG = h->KG_dn;
     StageTimer tdn(h, LMOE_STAGE_EXPERT_DOWN, st);
     LMOE_TRY(launch_moe_down(q, BNm, h->num_sms, st));

@@ -59,6 +59,10 @@ struct DispatchBufs {
   int* err;
 };
 constexpr int kDispatchChunk = 256;
+// Batches of at most this many assignments are dispatched by one kernel;
+// larger ones by the three-kernel chunked path.
+constexpr int kSmallDispatch = 8192;
+inline int dispatch_launches(int assignments) { return assignments <= kSmallDispatch ? 1 : 3; }
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, const DispatchBufs& b,
                             cudaStream_t s);
 
@@ -80,7 +84,9 @@ struct MoeGemmParams {
   const float* G;                // [T*k] routing weights (down pass)
   int* err;
   int N_out;                     // output features per expert (F for gate/up, din for down)
-  int MT;                        // ceil(N_out / 128)
+  int MT;                        // work-item columns per expert tile: 128-feature tiles (gate/up) or
+                                 // 256-row pairs (down)
+  int MTa;                       // 128-row tiles per expert in the scale-atom layout
   int KG;                        // Kp / 128
   // gate/up epilogue: h written as hi/lo E4M3 + scale atoms for the down pass
   uint8_t* hq;                   // [2*Ppad][Fp]

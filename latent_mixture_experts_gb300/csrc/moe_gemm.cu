@@ -8,14 +8,16 @@
 // two columns of the same MMA, so the weights are read from shared memory
 // once and the sum of the two columns restores ~16-bit activation precision.
 //
-// One work item = (expert tile of <= BN assignments, 128 output features).
+// One work item = (expert tile of <= BN assignments, 256 weight rows): the
+// gate and up rows of 128 features, or 256 consecutive down-projection rows.
 // A persistent grid walks the device-side tile list written by the dispatch
 // step.  Warp roles: 0 = TMA producer, 1 = MMA issuer, 2..5 = epilogue.
 //
 //   gate/up pass: two accumulators (gate rows, up rows of the same 128
 //     features), epilogue h = SiTU(g, u) (or SwiGLU), written back as hi/lo
 //     E4M3 for the down pass (Kimi K3 card, routed-expert steps).
-//   down pass: one accumulator, epilogue multiplies by the routing weight
+//   down pass: two accumulators (rows 256m.. and 256m+128..), epilogue
+//     multiplies by the routing weight
 //     G_i and stores the expert output of that assignment (moe_infer's
 //     weighted sum is finished by the combine kernel in slot order).
 #include "common.cuh"
@@ -33,20 +35,22 @@ struct MoeCfg {
   static constexpr int N = 2 * BN;                   // MMA N: hi/lo columns of BN assignments
   static constexpr int NA = (N + 127) / 128;         // 128-column scale atoms of B
   static constexpr int kA = 16384;                   // 128 rows x 128 FP4 codes, 16-byte slots
-  static constexpr int kNA = GU ? 2 : 1;             // A operands per stage
+  static constexpr int kNA = 2;                      // A operands per stage (gate+up, or two down tiles)
   static constexpr int kB = N * 128;                 // N rows x 128 E4M3 codes
+  static constexpr int kTile = kNA * kA + kB;        // swizzled tiles of one stage (multiple of 1024)
   static constexpr int kSfa = 512;
   static constexpr int kSfb = NA * 512;
-  static constexpr int kStage = (kNA * kA + kB + kNA * kSfa + kSfb + 1023) / 1024 * 1024;
-  static constexpr int kTx = kNA * 8192 + kB + kNA * kSfa + kSfb;    // bytes each stage's copies deliver
-  static constexpr int kStages = GU ? (BN >= 64 ? 4 : 5) : (BN >= 64 ? 6 : 8);
-  static constexpr int kSmem = kStages * kStage + 1024;
-  static constexpr int kAcc = kNA * N;                 // accumulator columns
-  static constexpr int kSfCols = kNA * 4 + NA * 4;     // scale columns per stage
-  static constexpr int kTmemUsed = kAcc + kStages * kSfCols;
+  static constexpr int kSf = kNA * kSfa + kSfb;      // scale atoms of one stage
+  static constexpr int kTx = kNA * 8192 + kB + kSf;  // bytes each stage's copies deliver
+  static constexpr int kStages = BN >= 64 ? 4 : 6;
+  static constexpr int kSmem = kStages * (kTile + kSf) + 1024;
+  static constexpr int kAcc = kNA * N;               // accumulator columns of one buffer
+  static constexpr int kSfCols = kNA * 4 + NA * 4;   // scale columns per stage
+  static constexpr int kAccBufs = (2 * kAcc + kStages * kSfCols <= 512) ? 2 : 1;
+  static constexpr int kTmemUsed = kAccBufs * kAcc + kStages * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
-  static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(kTile % 1024 == 0, "tiles keep 1024-byte alignment");
   static_assert(kTmemUsed <= 512, "tensor memory budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -57,13 +61,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-
 template <int BN, bool GU>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
   using C = MoeCfg<BN, GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  __shared__ uint64_t full[C::kStages], empty[C::kStages], acc_full, acc_empty;
+  uint8_t* sf_region = sm + C::kStages * C::kTile;
+  __shared__ uint64_t full[C::kStages], empty[C::kStages], acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -72,8 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, kEpiWarps * 32);
+    for (int i = 0; i < C::kAccBufs; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps * 32);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -89,25 +95,32 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const int total = ntiles * p.MT;
   const int KG = p.KG;
 
-  // stage sub-buffers
-  auto st_a = [&](int s, int j) { return sm + s * C::kStage + j * C::kA; };
-  auto st_b = [&](int s) { return sm + s * C::kStage + C::kNA * C::kA; };
-  auto st_sfa = [&](int s, int j) { return sm + s * C::kStage + C::kNA * C::kA + C::kB + j * C::kSfa; };
-  auto st_sfb = [&](int s) { return sm + s * C::kStage + C::kNA * C::kA + C::kB + C::kNA * C::kSfa; };
+  // stage sub-buffers: swizzled tiles first, all scale atoms after them
+  auto st_a = [&](int s, int j) { return sm + s * C::kTile + j * C::kA; };
+  auto st_b = [&](int s) { return sm + s * C::kTile + C::kNA * C::kA; };
+  auto st_sfa = [&](int s, int j) { return sf_region + s * C::kSf + j * C::kSfa; };
+  auto st_sfb = [&](int s) { return sf_region + s * C::kSf + C::kNA * C::kSfa; };
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&p.a_gate);
       if (GU) tma_prefetch_desc(&p.a_up);
       tma_prefetch_desc(&p.b);
+      const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
+      const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate;
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const int4 tile = p.tiles[w / p.MT];
         const int mt = w % p.MT;
         const int e = tile.x, row0 = tile.y;
-        const int arow = e * p.N_out + mt * 128;
-        const size_t sfa_idx = (static_cast<size_t>(e) * p.MT + mt) * KG;
+        // weight rows of the two A operands and their scale-atom tiles
+        const int t0 = GU ? mt : 2 * mt;
+        const int t1 = GU ? mt : min(2 * mt + 1, p.MTa - 1);
+        const int arow0 = e * p.N_out + t0 * 128;
+        const int arow1 = GU ? arow0 : arow0 + 128;
+        const size_t sfa0 = (static_cast<size_t>(e) * p.MTa + t0) * KG;
+        const size_t sfa1i = (static_cast<size_t>(e) * p.MTa + t1) * KG;
         const size_t sfb_idx = static_cast<size_t>(row0 / BN) * KG;
         for (int g = 0; g < KG; ++g, ++it) {
           const int s = it % C::kStages;
@@ -116,11 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             break;
           }
           mbar_arrive_expect_tx(&full[s], C::kTx);
-          tma_load_2d(st_a(s, 0), &p.a_gate, &full[s], g * 128, arow);
-          if (GU) tma_load_2d(st_a(s, 1), &p.a_up, &full[s], g * 128, arow);
+          tma_load_2d(st_a(s, 0), &p.a_gate, &full[s], g * 128, arow0);
+          tma_load_2d(st_a(s, 1), map1, &full[s], g * 128, arow1);
           tma_load_2d(st_b(s), &p.b, &full[s], g * 128, 2 * row0);
-          bulk_g2s(st_sfa(s, 0), p.sfa_gate + (sfa_idx + g) * 512, 512, &full[s]);
-          if (GU) bulk_g2s(st_sfa(s, 1), p.sfa_up + (sfa_idx + g) * 512, 512, &full[s]);
+          bulk_g2s(st_sfa(s, 0), p.sfa_gate + (sfa0 + g) * 512, 512, &full[s]);
+          bulk_g2s(st_sfa(s, 1), sfa1 + (sfa1i + g) * 512, 512, &full[s]);
           bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, C::kSfb, &full[s]);
         }
       }
@@ -129,10 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (lane == 0) {
       uint32_t it = 0, titer = 0;
       bool ok = true;
-      const uint32_t d_gate = tbase, d_up = tbase + C::N;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++titer) {
-        if (titer > 0 && !mbar_wait(&acc_empty, (titer - 1) & 1, p.err, kErrTimeout)) break;
+        const int b = titer % C::kAccBufs;
+        const uint32_t use = titer / C::kAccBufs;
+        if (use > 0 && !mbar_wait(&acc_empty[b], (use - 1) & 1, p.err, kErrTimeout)) break;
         tc_fence_after();
+        const uint32_t d_gate = tbase + b * C::kAcc, d_up = d_gate + C::N;
         for (int g = 0; g < KG; ++g, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
@@ -140,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t sf = tbase + C::kAcc + s * C::kSfCols;
+          const uint32_t sf = tbase + C::kAccBufs * C::kAcc + s * C::kSfCols;
           const uint32_t sfa_g = sf, sfa_u = sf + 4, sfb = sf + 4 * C::kNA;
           tmem_cp_32x128b_x4(sfa_g, sdesc_noswz(smem_u32(st_sfa(s, 0)), 16, 128));
-          if (GU) tmem_cp_32x128b_x4(sfa_u, sdesc_noswz(smem_u32(st_sfa(s, 1)), 16, 128));
+          tmem_cp_32x128b_x4(sfa_u, sdesc_noswz(smem_u32(st_sfa(s, 1)), 16, 128));
 #pragma unroll
           for (int a = 0; a < C::NA; ++a)
             tmem_cp_32x128b_x4(sfb + 4 * a, sdesc_noswz(smem_u32(st_sfb(s)) + 512 * a, 16, 128));
@@ -155,11 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             const uint32_t idesc = idesc_mxf8f6f4(128, C::N, 5, 0, kb, kb);
             const uint32_t acc = (g | kb) != 0;
             mma_mxf8f6f4(d_gate, sdesc_sw128(ag + 32 * kb), sdesc_sw128(bb + 32 * kb), idesc, sfa_g, sfb, acc);
-            if (GU) mma_mxf8f6f4(d_up, sdesc_sw128(au + 32 * kb), sdesc_sw128(bb + 32 * kb), idesc, sfa_u, sfb, acc);
+            mma_mxf8f6f4(d_up, sdesc_sw128(au + 32 * kb), sdesc_sw128(bb + 32 * kb), idesc, sfa_u, sfb, acc);
           }
           mma_commit(&empty[s]);
         }
-        mma_commit(&acc_full);
+        mma_commit(&acc_full[b]);
       }
     }
   } else {
@@ -167,24 +182,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     const int q = warp & 3;
     uint32_t titer = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++titer) {
-      if (!mbar_wait(&acc_full, titer & 1, p.err, kErrTimeout)) break;
+      const int b = titer % C::kAccBufs;
+      const uint32_t use = titer / C::kAccBufs;
+      if (!mbar_wait(&acc_full[b], use & 1, p.err, kErrTimeout)) break;
       tc_fence_after();
       const int4 tile = p.tiles[w / p.MT];
       const int mt = w % p.MT;
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      const int f = mt * 128 + 32 * q + lane;          // output feature of this lane
+      const int f = (GU ? mt * 128 : mt * 256) + 32 * q + lane;   // output feature of this lane
       const bool f_ok = f < p.N_out;
-      const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+      const uint32_t acc_base = tbase + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAcc;
 #pragma unroll 1
       for (int j0 = 0; j0 < BN; j0 += 16) {
         if (j0 >= nrows) break;
         uint32_t rg[32];
-        tmem_ld16(tbase + lane_base + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&rg[0]));
-        tmem_ld16(tbase + lane_base + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rg[16]));
+        tmem_ld16(acc_base + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&rg[0]));
+        tmem_ld16(acc_base + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rg[16]));
         if constexpr (GU) {
           uint32_t ru[32];
-          tmem_ld16(tbase + lane_base + C::N + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&ru[0]));
-          tmem_ld16(tbase + lane_base + C::N + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ru[16]));
+          tmem_ld16(acc_base + C::N + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&ru[0]));
+          tmem_ld16(acc_base + C::N + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ru[16]));
           tmem_ld_wait();
           const int kblk = f >> 5;                         // 32-feature block = this warp
           const int g = kblk >> 2, kb = kblk & 3;
@@ -207,19 +224,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             }
           }
         } else {
+          uint32_t r2[32];
+          tmem_ld16(acc_base + C::N + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&r2[0]));
+          tmem_ld16(acc_base + C::N + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r2[16]));
           tmem_ld_wait();
+          const int f1 = f + 128;                          // row of the second down tile
+          const bool f1_ok = f1 < p.N_out;
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
             if (j >= nrows) continue;
             const int a = p.perm[p0 + j];
-            const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * p.G[a];
-            if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
+            const float gw = p.G[a];
+            float* ya = p.y + static_cast<size_t>(a) * p.N_out;
+            if (f_ok) ya[f] = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
+            if (f1_ok) ya[f1] = (__uint_as_float(r2[2 * jj]) + __uint_as_float(r2[2 * jj + 1])) * gw;
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty);
+      mbar_arrive(&acc_empty[b]);
     }
   }
   tc_fence_before();
@@ -238,55 +262,65 @@ cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
 }
 
 // ------------------------------------------------------ activation encode
-// One warp per assignment: x^c row of its token -> hi/lo E4M3 rows 2r, 2r+1
-// of the padded layout, scales into the staging image of the row's tile.
+// One warp per (token, 32-element block) of x^c: the hi/lo E4M3 codes are
+// computed once and written to the padded rows 2r, 2r+1 of each of the
+// token's k assignments; their scales go into the staging image of each
+// row's tile.
 __global__ void quant_gather_kernel(const float* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, uint8_t* __restrict__ xq,
                                     uint8_t* __restrict__ xsf) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int P = T * k;
-  if (warp >= P) return;
-  const int a = warp;
-  const int r = inv_pad[a];
-  const int t = a / k;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nblk = Kp / 32;
+  if (gw >= T * nblk) return;
+  const int t = gw / nblk, blk = gw % nblk;
+  const int c = blk * 32 + lane;
+  const float v = c < din ? xc[static_cast<size_t>(t) * din + c] : 0.0f;
+  const HiLo e = quant_hilo_warp(v);
   const int NA = (2 * BN + 127) / 128;
   const int KG = Kp / 128;
-  const float* row = xc + static_cast<size_t>(t) * din;
-  const int jt = r % BN;
-  uint8_t* atoms = xsf + static_cast<size_t>(r / BN) * KG * NA * 512;
-  for (int blk = 0; blk < Kp / 32; ++blk) {
-    const int c = blk * 32 + lane;
-    const float v = c < din ? row[c] : 0.0f;
-    const HiLo e = quant_hilo_warp(v);
-    xq[(2 * static_cast<size_t>(r)) * Kp + c] = e.q_hi;
-    xq[(2 * static_cast<size_t>(r) + 1) * Kp + c] = e.q_lo;
-    if (lane == 0) {
-      const int g = blk >> 2, kb = blk & 3;
-      const int n = 2 * jt;
-      uint8_t* at = atoms + static_cast<size_t>(g) * NA * 512;
-      at[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
-      at[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
-    }
+  const int g = blk >> 2, kb = blk & 3;
+  for (int j = 0; j < k; ++j) {
+    const size_t r = static_cast<size_t>(inv_pad[static_cast<size_t>(t) * k + j]);
+    xq[(2 * r) * Kp + c] = e.q_hi;
+    xq[(2 * r + 1) * Kp + c] = e.q_lo;
+  }
+  for (int j = lane; j < k; j += 32) {
+    const int r = inv_pad[static_cast<size_t>(t) * k + j];
+    const int n = 2 * (r % BN);
+    uint8_t* at = xsf + (static_cast<size_t>(r / BN) * KG + g) * NA * 512;
+    at[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
+    at[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
   }
 }
 
 // One block per token: u = sum over the token's k slots in slot order, then
 // RMSNorm (Kimi K3 card code: routed_expert_norm between the sum and the
-// up-projection).
-__global__ void combine_norm_kernel(const float* __restrict__ y, int T, int k, int l,
-                                    const __nv_bfloat16* __restrict__ w, int use_norm, float eps,
-                                    float* __restrict__ u_out, __nv_bfloat16* __restrict__ u_hat) {
-  extern __shared__ float cn_u[];
+// up-projection).  float4 loads; the k slot loads of an element are
+// independent so they overlap.
+__global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restrict__ y, int T, int k, int l,
+                                                           const __nv_bfloat16* __restrict__ w, int use_norm,
+                                                           float eps, float* __restrict__ u_out,
+                                                           __nv_bfloat16* __restrict__ u_hat) {
+  extern __shared__ float4 cn_u4[];
   __shared__ float red[32];
   const int t = blockIdx.x;
-  const float* yt = y + static_cast<size_t>(t) * k * l;
+  const int l4 = l >> 2;
+  const float4* yt = reinterpret_cast<const float4*>(y + static_cast<size_t>(t) * k * l);
+  float4* ut = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * l);
   float ss = 0.f;
-  for (int i = threadIdx.x; i < l; i += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < k; ++j) acc += yt[static_cast<size_t>(j) * l + i];
-    cn_u[i] = acc;
-    u_out[static_cast<size_t>(t) * l + i] = acc;
-    ss += acc * acc;
+  for (int i = threadIdx.x; i < l4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const float4 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    cn_u4[i] = acc;
+    ut[i] = acc;
+    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
   }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -298,9 +332,17 @@ __global__ void combine_norm_kernel(const float* __restrict__ y, int T, int k, i
   }
   __syncthreads();
   const float rs = use_norm ? rsqrtf(red[0] / static_cast<float>(l) + eps) : 1.0f;
-  for (int i = threadIdx.x; i < l; i += blockDim.x) {
-    const float wv = use_norm ? __bfloat162float(w[i]) : 1.0f;
-    u_hat[static_cast<size_t>(t) * l + i] = __float2bfloat16_rn(wv * cn_u[i] * rs);
+  __nv_bfloat162* ot = reinterpret_cast<__nv_bfloat162*>(u_hat + static_cast<size_t>(t) * l);
+  const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(w);
+  for (int i = threadIdx.x; i < l4; i += blockDim.x) {
+    const float4 a = cn_u4[i];
+    float2 w01 = make_float2(1.f, 1.f), w23 = make_float2(1.f, 1.f);
+    if (use_norm) {
+      w01 = __bfloat1622float2(w2[2 * i]);
+      w23 = __bfloat1622float2(w2[2 * i + 1]);
+    }
+    ot[2 * i] = __floats2bfloat162_rn(w01.x * a.x * rs, w01.y * a.y * rs);
+    ot[2 * i + 1] = __floats2bfloat162_rn(w23.x * a.z * rs, w23.y * a.w * rs);
   }
 }
 
@@ -356,11 +398,11 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
                                 uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
-  const int P = T * k;
-  if (P <= 0) return cudaSuccess;
+  if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
-  quant_gather_kernel<<<(P + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, s>>>(
-      xc, T, k, din, Kp, inv_pad, BN, xq, xsf);
+  const long long warps = static_cast<long long>(T) * (Kp / 32);
+  quant_gather_kernel<<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block), 32 * warps_per_block,
+                        0, s>>>(xc, T, k, din, Kp, inv_pad, BN, xq, xsf);
   return cudaGetLastError();
 }
 
@@ -372,7 +414,7 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void*
     cudaError_t e = cudaFuncSetAttribute(combine_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  combine_norm_kernel<<<T, 256, smem, s>>>(y, T, k, l, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
+  combine_norm_kernel<<<T, 512, smem, s>>>(y, T, k, l, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
                                           static_cast<__nv_bfloat16*>(u_hat));
   return cudaGetLastError();
 }

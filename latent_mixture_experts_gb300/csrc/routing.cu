@@ -18,22 +18,22 @@ namespace lmoe {
 
 namespace {
 
-constexpr int kTopkWarps = 4;
+constexpr int kTopkThreads = 256;
 
-// One warp per token.  Scores live in shared memory; each selection round
-// every lane finds its best candidate and the warp reduces (value, index).
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ part, int splits, int T,
-                                                               int E, const float* __restrict__ bias, int k,
-                                                               float scale, int32_t* __restrict__ idx,
-                                                               float* __restrict__ G, float* __restrict__ z_out) {
+// One block per token: all threads sum the split-K partial logits (coalesced
+// over experts) and form s and c in shared memory; warp 0 then selects the
+// k largest c one at a time, each round reducing (value, index) across the
+// warp with ties to the lower index.
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ part, int splits, int T,
+                                                            int E, const float* __restrict__ bias, int k,
+                                                            float scale, int32_t* __restrict__ idx,
+                                                            float* __restrict__ G, float* __restrict__ z_out) {
   extern __shared__ float tk_smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTopkWarps + warp;
-  if (t >= T) return;
-  float* c = tk_smem + static_cast<size_t>(warp) * 2 * E;
-  float* sg = c + E;
+  float* c = tk_smem;
+  float* sg = tk_smem + E;
+  const int t = blockIdx.x;
   const size_t plane = static_cast<size_t>(T) * E;
-  for (int e = lane; e < E; e += 32) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float z = 0.f;
     for (int s = 0; s < splits; ++s) z += part[s * plane + static_cast<size_t>(t) * E + e];
     z_out[static_cast<size_t>(t) * E + e] = z;
@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
     sg[e] = sv;
     c[e] = sv + bias[e];
   }
-  __syncwarp();
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   float sel_s[32];
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
@@ -75,6 +77,111 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
     for (int j = 0; j < k; ++j) sum += sel_s[j];
     const float inv = scale / sum;
     for (int j = 0; j < k; ++j) G[static_cast<size_t>(t) * k + j] = sel_s[j] * inv;
+  }
+}
+
+// Whole dispatch in one block, for batches of at most kSmallDispatch
+// assignments: shared-memory histogram, block scans over the experts, then
+// one warp walks the assignments in order for the stable placement.
+
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __restrict__ idx, int P, int E, int BN,
+                                                              int32_t* __restrict__ counts,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ perm,
+                                                              int32_t* __restrict__ inv_pad,
+                                                              int32_t* __restrict__ tile_off,
+                                                              int4* __restrict__ tiles, int32_t* __restrict__ ntiles,
+                                                              int* err) {
+  __shared__ int32_t hist[kMaxExperts];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  __shared__ int32_t s_toff[kMaxExperts + 1];
+  __shared__ int32_t s_tst[kMaxExperts + 1];
+  __shared__ int32_t wsum[3][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  for (int a = tid; a < P; a += blockDim.x) {
+    const int e = idx[a];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else if (err) atomicExch(err + 1, 1);
+  }
+  __syncthreads();
+  // exclusive scans of (count, padded count, tiles): thread owns experts 2*tid, 2*tid+1
+  int v[2][3];
+  int loc[3] = {0, 0, 0};
+  for (int q = 0; q < 2; ++q) {
+    const int e = 2 * tid + q;
+    const int c = e < E ? hist[e] : 0;
+    const int n = (c + BN - 1) / BN;
+    v[q][0] = c;
+    v[q][1] = n * BN;
+    v[q][2] = n;
+    for (int m = 0; m < 3; ++m) loc[m] += v[q][m];
+  }
+  int incl[3];
+  for (int m = 0; m < 3; ++m) {
+    int x = loc[m];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    incl[m] = x;
+    if (lane == 31) wsum[m][warp] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int m = 0; m < 3; ++m) {
+      int x = lane < (blockDim.x >> 5) ? wsum[m][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      wsum[m][lane] = x;   // inclusive over warps
+    }
+  }
+  __syncthreads();
+  int base[3];
+  for (int m = 0; m < 3; ++m) base[m] = (warp ? wsum[m][warp - 1] : 0) + incl[m] - loc[m];
+  for (int q = 0; q < 2; ++q) {
+    const int e = 2 * tid + q;
+    if (e < E) {
+      s_off[e] = base[0];
+      s_toff[e] = base[1];
+      s_tst[e] = base[2];
+      counts[e] = v[q][0];
+      offsets[e] = base[0];
+      tile_off[e] = base[1];
+      for (int i = 0; i < v[q][2]; ++i)
+        tiles[base[2] + i] = make_int4(e, base[1] + i * BN, min(BN, v[q][0] - i * BN), base[0] + i * BN);
+    }
+    for (int m = 0; m < 3; ++m) base[m] += v[q][m];
+  }
+  if (tid == blockDim.x - 1) {
+    offsets[E] = base[0];
+    tile_off[E] = base[1];
+    *ntiles = base[2];
+  }
+  __syncthreads();
+  // stable placement: warp 0 walks the assignments in order, 32 at a time
+  if (warp == 0) {
+    for (int a0 = 0; a0 < P; a0 += 32) {
+      const int a = a0 + lane;
+      int e = a < P ? idx[a] : -1;
+      if (e < 0 || e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int b = e >= 0 ? s_off[e] : 0;
+      __syncwarp();
+      if (e >= 0) {
+        const int pidx = b + rank;
+        perm[pidx] = a;
+        inv_pad[a] = s_toff[e] + (pidx - offsets[e]);
+        if (rank == 0) s_off[e] = b + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -183,14 +290,8 @@ __global__ void __launch_bounds__(32) dispatch_scatter_kernel(const int32_t* __r
 cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const float* bias, int k,
                         float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
-  const size_t smem = static_cast<size_t>(kTopkWarps) * 2 * E * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logit_part, splits, T, E, bias, k, routed_scale, idx, G,
-                                                     z_out);
+  const size_t smem = 2 * static_cast<size_t>(E) * sizeof(float);
+  topk_kernel<<<T, kTopkThreads, smem, s>>>(logit_part, splits, T, E, bias, k, routed_scale, idx, G, z_out);
   return cudaGetLastError();
 }
 
@@ -198,6 +299,11 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
                             cudaStream_t s) {
   const int P = T * k;
   if (P <= 0) return cudaSuccess;
+  if (P <= kSmallDispatch) {
+    dispatch_small_kernel<<<1, 1024, 0, s>>>(idx, P, E, BN, b.counts, b.offsets, b.perm, b.inv_pad, b.tile_off,
+                                             b.tiles, b.ntiles, b.err);
+    return cudaGetLastError();
+  }
   const int nchunks = (P + kDispatchChunk - 1) / kDispatchChunk;
   const size_t hsmem = static_cast<size_t>(E) * sizeof(int32_t);
   dispatch_count_kernel<<<nchunks, 256, hsmem, s>>>(idx, P, E, b.blockcnt, b.err);

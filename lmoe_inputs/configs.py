@@ -69,6 +69,9 @@ WORKLOADS = {
     "k3_prefill_t8192": Workload("k3_prefill_t8192", K3, T=8192, seed=2, bias="zipf"),
     "k2_t4096": Workload("k2_t4096", K2, T=4096, seed=3),
 }
+# Kimi-K3 shapes with 64 experts (1.1 GB of expert weights): the small case
+# for detailed profiler captures of the same kernels.
+WORKLOADS["k3_e64_t8"] = Workload("k3_e64_t8", replace(K3, n_experts=64), T=8, seed=6)
 SWEEP_T = (1, 8, 32, 128, 512, 2048)
 for _t in SWEEP_T:
     WORKLOADS[f"k3_sweep_t{_t}"] = Workload(f"k3_sweep_t{_t}", K3, T=_t, seed=4)
