@@ -28,7 +28,7 @@ struct lmoe_ctx {
   lmoe_weights w;
   int dev = 0, num_sms = 148;
   int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
-  int Kp = 0, Fp = 0, MT_gu = 0, MT_dn = 0, KG_gu = 0, KG_dn = 0;
+  int Kp = 0, Fp = 0, MT_gu = 0, MT_dn = 0, KG_gu = 0, KG_dn = 0, MTa_gu = 0, MTa_dn = 0;
   int Tm = 0, Pm = 0, Ppad = 0, max_tiles = 0, nchunks_max = 0;
   // device memory
   void* pool = nullptr;
@@ -53,7 +53,8 @@ struct lmoe_ctx {
   const uint8_t *codes_gate = nullptr, *codes_up = nullptr, *codes_down = nullptr;
   uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
   // static tensor maps
-  CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd, m_exg, m_exu, m_exd;
+  CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
+  CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
   int last_T = 0;
   int last_launches = 0;
   // per-stage event timing
@@ -106,9 +107,9 @@ bool map_bf16(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, K, rows, static_cast<uint64_t>(K) * 2, 64, box_rows,
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
-bool map_fp4(CUtensorMap* m, const void* base, int K, long long rows) {
-  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, base, K, rows, static_cast<uint64_t>(K) / 2, 128, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+bool map_fp4(CUtensorMap* m, const void* base, int K, long long rows, int box_rows) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, base, K, rows, static_cast<uint64_t>(K) / 2, 128,
+                      box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 bool map_u8(CUtensorMap* m, const void* base, int K, long long rows, int box_rows) {
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, K, rows, K, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -302,6 +303,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->Fp = static_cast<int>(align_up(h->F, 128));
   h->MT_gu = h->Fp / 128;
   h->MT_dn = ceil_div(h->din, 128);
+  h->MTa_gu = (h->MT_gu + 1) / 2 * 2;
+  h->MTa_dn = (h->MT_dn + 3) / 4 * 4;   // the down pass copies the atoms of up to four 128-row tiles per stage
   h->KG_gu = h->Kp / 128;
   h->KG_dn = h->Fp / 128;
   h->Tm = cfg->max_tokens;
@@ -353,9 +356,9 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);
     h->x_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
     h->out_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
-    h->sfa_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_gu * h->KG_gu * 512, base);
-    h->sfa_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_gu * h->KG_gu * 512, base);
-    h->sfa_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MT_dn * h->KG_dn * 512, base);
+    h->sfa_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512, base);
+    h->sfa_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512, base);
+    h->sfa_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512, base);
     if (pad_gu) {
       h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
       h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
@@ -381,9 +384,9 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const uint8_t* sg = static_cast<const uint8_t*>(w->ex_gate_s);
   const uint8_t* su = static_cast<const uint8_t*>(w->ex_up_s);
   const uint8_t* sd = static_cast<const uint8_t*>(w->ex_down_s);
-  if (launch_relayout_sfa(sg, h->E, h->F, h->din / 32, h->MT_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
-      launch_relayout_sfa(su, h->E, h->F, h->din / 32, h->MT_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
-      launch_relayout_sfa(sd, h->E, h->din, h->F / 32, h->MT_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess)
+  if (launch_relayout_sfa(sg, h->E, h->F, h->din / 32, h->MTa_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
+      launch_relayout_sfa(su, h->E, h->F, h->din / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
+      launch_relayout_sfa(sd, h->E, h->din, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess)
     return fail(LMOE_ERR_CUDA);
   h->codes_gate = w->ex_gate_q;
   h->codes_up = w->ex_up_q;
@@ -409,9 +412,12 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     ok &= map_bf16(&h->m_shu, w->sh_up, h->d, h->Fs, 128);
     ok &= map_bf16(&h->m_shd, w->sh_down, h->Fs, h->d, 128);
   }
-  ok &= map_fp4(&h->m_exg, h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F);
-  ok &= map_fp4(&h->m_exu, h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F);
-  ok &= map_fp4(&h->m_exd, h->codes_down, h->Fp, static_cast<long long>(h->E) * h->din);
+  for (int i = 0; i < 2; ++i) {
+    const int rows = 128 << i;
+    ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+    ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+    ok &= map_fp4(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->din, rows);
+  }
   if (!ok) return fail(LMOE_ERR_CUDA);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
   if (cudaGetLastError() != cudaSuccess) return fail(LMOE_ERR_CUDA);
@@ -506,8 +512,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
-    p.a_gate = h->m_exg;
-    p.a_up = h->m_exu;
+    const int RB = moe_rows_per_item(BNm);
+    const int mi = RB == 256 ? 1 : 0;
+    p.a_gate = h->m_exg[mi];
+    p.a_up = h->m_exu[mi];
     if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
     p.sfa_gate = h->sfa_gate;
     p.sfa_up = h->sfa_up;
@@ -518,8 +526,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.G = h->G;
     p.err = h->err;
     p.N_out = h->F;
-    p.MT = h->MT_gu;
-    p.MTa = h->MT_gu;
+    p.MT = ceil_div(h->F, RB);
+    p.MTa = h->MTa_gu;
     p.KG = h->KG_gu;
     p.hq = h->hq;
     p.hsf = h->hsf;
@@ -533,14 +541,14 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     ++launches;
     tgu.done();
     MoeGemmParams q = p;
-    q.a_gate = h->m_exd;
+    q.a_gate = h->m_exd[mi];
     if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
     q.sfa_gate = h->sfa_down;
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
     q.N_out = din;
-    q.MT = (h->MT_dn + 1) / 2;
-    q.MTa = h->MT_dn;
+    q.MT = ceil_div(din, 2 * RB);
+    q.MTa = h->MTa_dn;
     q.KG = h->KG_dn;
     StageTimer tdn(h, LMOE_STAGE_EXPERT_DOWN, st);
     LMOE_TRY(launch_moe_down(q, BNm, h->num_sms, st));

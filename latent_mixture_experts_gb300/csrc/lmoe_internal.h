@@ -73,9 +73,15 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
                                 uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 
+// Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
+// 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
+// prefill keep 128-row items so two accumulators fit tensor memory.
+__host__ __device__ constexpr int moe_rows_per_item(int BN) { return BN >= 64 ? 128 : 256; }
+
 struct MoeGemmParams {
-  CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp]; activations [2*Ppad][Kp]
-  const uint8_t* sfa_gate;       // weight scale atoms [E][MT][G][512]
+  CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp] (boxes of moe_rows_per_item rows);
+                                 // activations [2*Ppad][Kp]
+  const uint8_t* sfa_gate;       // weight scale atoms [E][KG][MTa][512]
   const uint8_t* sfa_up;
   const uint8_t* sfb;            // activation scale atoms [Ppad/BN][G][NA][512]
   const int4* tiles;
@@ -84,9 +90,8 @@ struct MoeGemmParams {
   const float* G;                // [T*k] routing weights (down pass)
   int* err;
   int N_out;                     // output features per expert (F for gate/up, din for down)
-  int MT;                        // work-item columns per expert tile: 128-feature tiles (gate/up) or
-                                 // 256-row pairs (down)
-  int MTa;                       // 128-row tiles per expert in the scale-atom layout
+  int MT;                        // work-item columns per expert tile: ceil(N_out / rows per item)
+  int MTa;                       // 128-row tiles per (expert, k-group) in the scale-atom layout (even)
   int KG;                        // Kp / 128
   // gate/up epilogue: h written as hi/lo E4M3 + scale atoms for the down pass
   uint8_t* hq;                   // [2*Ppad][Fp]
@@ -105,7 +110,7 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void*
                                 float* u, void* u_hat, cudaStream_t s);
 
 // Create-time repacking of the expert weights.
-cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MT, int KG, uint8_t* atoms,
+cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,
                                 cudaStream_t st);
 cudaError_t launch_pad_codes(const uint8_t* q, int E, int N, int K, int Kp, uint8_t* out, cudaStream_t st);
 

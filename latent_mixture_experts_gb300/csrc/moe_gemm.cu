@@ -34,18 +34,22 @@ template <int BN, bool GU>
 struct MoeCfg {
   static constexpr int N = 2 * BN;                   // MMA N: hi/lo columns of BN assignments
   static constexpr int NA = (N + 127) / 128;         // 128-column scale atoms of B
-  static constexpr int kA = 16384;                   // 128 rows x 128 FP4 codes, 16-byte slots
-  static constexpr int kNA = 2;                      // A operands per stage (gate+up, or two down tiles)
+  static constexpr int RB = moe_rows_per_item(BN);   // weight rows per work item and TMA box
+  static constexpr int kTiles = RB / 128;            // 128-row MMA tiles per box
+  static constexpr int kBoxes = 2;                   // A boxes per stage: gate + up, or two down boxes
+  static constexpr int IR = GU ? RB : 2 * RB;        // weight rows of one work item
+  static constexpr int kNAcc = kBoxes * kTiles;      // accumulators per work item
+  static constexpr int kA = RB * 128;                // one box: RB rows x 128 FP4 codes in 16-byte slots
   static constexpr int kB = N * 128;                 // N rows x 128 E4M3 codes
-  static constexpr int kTile = kNA * kA + kB;        // swizzled tiles of one stage (multiple of 1024)
-  static constexpr int kSfa = 512;
+  static constexpr int kTile = kBoxes * kA + kB;     // swizzled tiles of one stage (multiple of 1024)
+  static constexpr int kSfa = kTiles * 512;          // scale atoms of one box (adjacent in memory)
   static constexpr int kSfb = NA * 512;
-  static constexpr int kSf = kNA * kSfa + kSfb;      // scale atoms of one stage
-  static constexpr int kTx = kNA * 8192 + kB + kSf;  // bytes each stage's copies deliver
-  static constexpr int kStages = BN >= 64 ? 4 : 6;
+  static constexpr int kSf = kBoxes * kSfa + kSfb;   // scale atoms of one stage
+  static constexpr int kTx = kBoxes * (kA / 2) + kB + kSf;   // bytes the stage's copies deliver
+  static constexpr int kStages = RB == 256 ? 3 : 4;
   static constexpr int kSmem = kStages * (kTile + kSf) + 1024;
-  static constexpr int kAcc = kNA * N;               // accumulator columns of one buffer
-  static constexpr int kSfCols = kNA * 4 + NA * 4;   // scale columns per stage
+  static constexpr int kAcc = kNAcc * N;             // accumulator columns of one buffer
+  static constexpr int kSfCols = kNAcc * 4 + NA * 4; // scale columns per stage
   static constexpr int kAccBufs = (2 * kAcc + kStages * kSfCols <= 512) ? 2 : 1;
   static constexpr int kTmemUsed = kAccBufs * kAcc + kStages * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
@@ -61,6 +65,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+
 template <int BN, bool GU>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
   using C = MoeCfg<BN, GU>;
@@ -97,30 +102,28 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 
   // stage sub-buffers: swizzled tiles first, all scale atoms after them
   auto st_a = [&](int s, int j) { return sm + s * C::kTile + j * C::kA; };
-  auto st_b = [&](int s) { return sm + s * C::kTile + C::kNA * C::kA; };
+  auto st_b = [&](int s) { return sm + s * C::kTile + C::kBoxes * C::kA; };
   auto st_sfa = [&](int s, int j) { return sf_region + s * C::kSf + j * C::kSfa; };
-  auto st_sfb = [&](int s) { return sf_region + s * C::kSf + C::kNA * C::kSfa; };
+  auto st_sfb = [&](int s) { return sf_region + s * C::kSf + C::kBoxes * C::kSfa; };
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&p.a_gate);
       if (GU) tma_prefetch_desc(&p.a_up);
       tma_prefetch_desc(&p.b);
-      const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
-      const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate;
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const int4 tile = p.tiles[w / p.MT];
         const int mt = w % p.MT;
         const int e = tile.x, row0 = tile.y;
-        // weight rows of the two A operands and their scale-atom tiles
-        const int t0 = GU ? mt : 2 * mt;
-        const int t1 = GU ? mt : min(2 * mt + 1, p.MTa - 1);
-        const int arow0 = e * p.N_out + t0 * 128;
-        const int arow1 = GU ? arow0 : arow0 + 128;
-        const size_t sfa0 = (static_cast<size_t>(e) * p.MTa + t0) * KG;
-        const size_t sfa1i = (static_cast<size_t>(e) * p.MTa + t1) * KG;
+        // second box: the up rows of the same features, or the next RB down rows
+        const int arow = e * p.N_out + mt * C::IR;
+        const int arow1 = GU ? arow : arow + C::RB;
+        const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
+        const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate + C::kSfa;
+        // atoms [E][KG][MTa][512]: the atoms of an item's tiles are adjacent
+        const size_t sfa_row = static_cast<size_t>(e) * KG;
         const size_t sfb_idx = static_cast<size_t>(row0 / BN) * KG;
         for (int g = 0; g < KG; ++g, ++it) {
           const int s = it % C::kStages;
@@ -128,12 +131,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             ok = false;
             break;
           }
+          const size_t sfa_off = ((sfa_row + g) * p.MTa + mt * (C::IR / 128)) * 512;
           mbar_arrive_expect_tx(&full[s], C::kTx);
-          tma_load_2d(st_a(s, 0), &p.a_gate, &full[s], g * 128, arow0);
+          tma_load_2d(st_a(s, 0), &p.a_gate, &full[s], g * 128, arow);
           tma_load_2d(st_a(s, 1), map1, &full[s], g * 128, arow1);
           tma_load_2d(st_b(s), &p.b, &full[s], g * 128, 2 * row0);
-          bulk_g2s(st_sfa(s, 0), p.sfa_gate + (sfa0 + g) * 512, 512, &full[s]);
-          bulk_g2s(st_sfa(s, 1), sfa1 + (sfa1i + g) * 512, 512, &full[s]);
+          bulk_g2s(st_sfa(s, 0), p.sfa_gate + sfa_off, C::kSfa, &full[s]);
+          bulk_g2s(st_sfa(s, 1), sfa1 + sfa_off, C::kSfa, &full[s]);
           bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, C::kSfb, &full[s]);
         }
       }
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const uint32_t use = titer / C::kAccBufs;
         if (use > 0 && !mbar_wait(&acc_empty[b], (use - 1) & 1, p.err, kErrTimeout)) break;
         tc_fence_after();
-        const uint32_t d_gate = tbase + b * C::kAcc, d_up = d_gate + C::N;
+        const uint32_t d0 = tbase + b * C::kAcc;
         for (int g = 0; g < KG; ++g, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
@@ -156,21 +160,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           }
           tc_fence_after();
           const uint32_t sf = tbase + C::kAccBufs * C::kAcc + s * C::kSfCols;
-          const uint32_t sfa_g = sf, sfa_u = sf + 4, sfb = sf + 4 * C::kNA;
-          tmem_cp_32x128b_x4(sfa_g, sdesc_noswz(smem_u32(st_sfa(s, 0)), 16, 128));
-          tmem_cp_32x128b_x4(sfa_u, sdesc_noswz(smem_u32(st_sfa(s, 1)), 16, 128));
+          const uint32_t sfb = sf + 4 * C::kNAcc;
+          // scale atoms -> TMEM: accumulator i = box j, tile t reads columns sf + 4i
+#pragma unroll
+          for (int i = 0; i < C::kNAcc; ++i)
+            tmem_cp_32x128b_x4(sf + 4 * i, sdesc_noswz(smem_u32(st_sfa(s, i / C::kTiles)) + 512 * (i % C::kTiles), 16, 128));
 #pragma unroll
           for (int a = 0; a < C::NA; ++a)
             tmem_cp_32x128b_x4(sfb + 4 * a, sdesc_noswz(smem_u32(st_sfb(s)) + 512 * a, 16, 128));
-          const uint32_t ag = smem_u32(st_a(s, 0));
-          const uint32_t au = smem_u32(st_a(s, 1));
           const uint32_t bb = smem_u32(st_b(s));
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
             const uint32_t idesc = idesc_mxf8f6f4(128, C::N, 5, 0, kb, kb);
             const uint32_t acc = (g | kb) != 0;
-            mma_mxf8f6f4(d_gate, sdesc_sw128(ag + 32 * kb), sdesc_sw128(bb + 32 * kb), idesc, sfa_g, sfb, acc);
-            mma_mxf8f6f4(d_up, sdesc_sw128(au + 32 * kb), sdesc_sw128(bb + 32 * kb), idesc, sfa_u, sfb, acc);
+#pragma unroll
+            for (int i = 0; i < C::kNAcc; ++i) {
+              const uint32_t a_addr = smem_u32(st_a(s, i / C::kTiles)) + (i % C::kTiles) * 16384 + 32 * kb;
+              mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + 32 * kb), idesc, sf + 4 * i, sfb, acc);
+            }
           }
           mma_commit(&empty[s]);
         }
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       }
     }
   } else {
-    // Epilogue warps: lane quarter q of TMEM = features 32q .. 32q+31 of the tile.
+    // Epilogue warps: lane quarter q of TMEM = rows 32q .. 32q+31 of each 128-row tile.
     const int q = warp & 3;
     uint32_t titer = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++titer) {
@@ -189,56 +196,57 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int4 tile = p.tiles[w / p.MT];
       const int mt = w % p.MT;
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      const int f = (GU ? mt * 128 : mt * 256) + 32 * q + lane;   // output feature of this lane
-      const bool f_ok = f < p.N_out;
       const uint32_t acc_base = tbase + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAcc;
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 16) {
-        if (j0 >= nrows) break;
-        uint32_t rg[32];
-        tmem_ld16(acc_base + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&rg[0]));
-        tmem_ld16(acc_base + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rg[16]));
-        if constexpr (GU) {
-          uint32_t ru[32];
-          tmem_ld16(acc_base + C::N + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&ru[0]));
-          tmem_ld16(acc_base + C::N + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ru[16]));
-          tmem_ld_wait();
-          const int kblk = f >> 5;                         // 32-feature block = this warp
-          const int g = kblk >> 2, kb = kblk & 3;
+      for (int t = 0; t < (GU ? C::kTiles : C::kNAcc); ++t) {
+        // A 256-row item can run past the last 128-row tile of h (whose rows
+        // the down pass reads up to Fp): nothing of such a tile is stored.
+        if (GU && mt * C::RB + t * 128 >= p.Fp) break;
+        const int f = mt * C::IR + t * 128 + 32 * q + lane;   // output feature of this lane
+        const bool f_ok = f < p.N_out;
+#pragma unroll 1
+        for (int j0 = 0; j0 < BN; j0 += 16) {
+          if (j0 >= nrows) break;
+          uint32_t rg[32];
+          const uint32_t a0 = acc_base + t * C::N + 2 * j0;
+          tmem_ld16(a0, *reinterpret_cast<uint32_t(*)[16]>(&rg[0]));
+          tmem_ld16(a0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rg[16]));
+          if constexpr (GU) {
+            uint32_t ru[32];
+            const uint32_t a1 = a0 + C::kTiles * C::N;        // up accumulator of the same tile
+            tmem_ld16(a1, *reinterpret_cast<uint32_t(*)[16]>(&ru[0]));
+            tmem_ld16(a1 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ru[16]));
+            tmem_ld_wait();
+            const int kblk = f >> 5;                         // 32-feature block = this warp
+            const int g = kblk >> 2, kb = kblk & 3;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = j0 + jj;
-            if (j >= nrows) continue;                      // warp-uniform
-            const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
-            const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
-            const float h = f_ok ? glu_act(gv, uv, p.act, p.b1, p.b2) : 0.0f;
-            const HiLo e = quant_hilo_warp(h);
-            const size_t r = static_cast<size_t>(row0) + j;
-            p.hq[(2 * r) * p.Fp + f] = e.q_hi;
-            p.hq[(2 * r + 1) * p.Fp + f] = e.q_lo;
-            if (lane == 0) {
-              const int n = 2 * j;                         // MMA column of the hi term in the down pass
-              uint8_t* atom = p.hsf + ((static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * C::NA) * 512;
-              atom[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
-              atom[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = j0 + jj;
+              if (j >= nrows) continue;                      // warp-uniform
+              const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
+              const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
+              const float h = f_ok ? glu_act(gv, uv, p.act, p.b1, p.b2) : 0.0f;
+              const HiLo e = quant_hilo_warp(h);
+              const size_t r = static_cast<size_t>(row0) + j;
+              p.hq[(2 * r) * p.Fp + f] = e.q_hi;
+              p.hq[(2 * r + 1) * p.Fp + f] = e.q_lo;
+              if (lane == 0) {
+                const int n = 2 * j;                         // MMA column of the hi term in the down pass
+                uint8_t* atom = p.hsf + ((static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * C::NA) * 512;
+                atom[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
+                atom[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
+              }
             }
-          }
-        } else {
-          uint32_t r2[32];
-          tmem_ld16(acc_base + C::N + 2 * j0, *reinterpret_cast<uint32_t(*)[16]>(&r2[0]));
-          tmem_ld16(acc_base + C::N + 2 * j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r2[16]));
-          tmem_ld_wait();
-          const int f1 = f + 128;                          // row of the second down tile
-          const bool f1_ok = f1 < p.N_out;
+          } else {
+            tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = j0 + jj;
-            if (j >= nrows) continue;
-            const int a = p.perm[p0 + j];
-            const float gw = p.G[a];
-            float* ya = p.y + static_cast<size_t>(a) * p.N_out;
-            if (f_ok) ya[f] = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
-            if (f1_ok) ya[f1] = (__uint_as_float(r2[2 * jj]) + __uint_as_float(r2[2 * jj + 1])) * gw;
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = j0 + jj;
+              if (j >= nrows) continue;
+              const int a = p.perm[p0 + j];
+              const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * p.G[a];
+              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
+            }
           }
         }
       }
@@ -346,17 +354,21 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restri
   }
 }
 
-__global__ void relayout_sfa_kernel(const uint8_t* __restrict__ s, int E, int N, int Kb, int MT, int KG,
+// Scale atoms [E][KG][MTa][512]: for expert e, k-group g (128 K values) and
+// 128-row tile t, line r0 holds for c = 0..3 the four k-block scales of row
+// 128t + 32c + r0.  Tiles of one k-group are adjacent, so a 256-row box's
+// two atoms arrive in one copy.  Rows past N and k-blocks past Kb read 127.
+__global__ void relayout_sfa_kernel(const uint8_t* __restrict__ s, int E, int N, int Kb, int MTa, int KG,
                                     uint8_t* __restrict__ atoms) {
-  const size_t total = static_cast<size_t>(E) * MT * KG * 512;
+  const size_t total = static_cast<size_t>(E) * KG * MTa * 512;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int b = static_cast<int>(i & 511);
     size_t rest = i >> 9;
+    const int mt = static_cast<int>(rest % MTa);
+    rest /= MTa;
     const int g = static_cast<int>(rest % KG);
-    rest /= KG;
-    const int mt = static_cast<int>(rest % MT);
-    const int e = static_cast<int>(rest / MT);
+    const int e = static_cast<int>(rest / KG);
     const int r0 = b >> 4, c = (b >> 2) & 3, kb = b & 3;
     const int n = mt * 128 + 32 * c + r0;
     const int kblk = 4 * g + kb;
@@ -419,10 +431,10 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void*
   return cudaGetLastError();
 }
 
-cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MT, int KG, uint8_t* atoms,
+cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,
                                 cudaStream_t st) {
-  const size_t total = static_cast<size_t>(E) * MT * KG * 512;
-  relayout_sfa_kernel<<<ew_grid(total), 256, 0, st>>>(s, E, N, Kb, MT, KG, atoms);
+  const size_t total = static_cast<size_t>(E) * MTa * KG * 512;
+  relayout_sfa_kernel<<<ew_grid(total), 256, 0, st>>>(s, E, N, Kb, MTa, KG, atoms);
   return cudaGetLastError();
 }
 
