@@ -41,6 +41,10 @@ UNIT = "tokens/s"
 EXPERT_BYTES = 17_547_264          # one K3 expert: 3 x 3584 x 3072 E2M1 codes + E8M0 scales
 DENSE_BYTES = 379_857_408          # K3 bf16 router, W_down, W_up, norm, shared MLP + fp32 bias
 TOKEN_IO_BYTES = 28_672            # x in + Delta out, bf16, per token
+# DRAM bytes per algorithmic byte of the gate/up expert kernel, from one ncu
+# capture of the current kernel (read + write 702.2 MB for 645 MB algorithmic).
+# Set to None when the kernel changes until it is captured again.
+GU_DRAM_PER_ALGO_BYTE = 1.089
 
 
 def peaks():
@@ -256,7 +260,11 @@ def run_ours(args):
                    "active_experts_mean": round(U_mean, 1)},
         "roofline": {"kernel": "moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm"], 4),
+                     "traffic": int(GU_DRAM_PER_ALGO_BYTE * gu_bytes) if GU_DRAM_PER_ALGO_BYTE else None,
+                     "traffic_source": "ncu dram__bytes_read+write of this kernel on the 64-expert K3-shaped case "
+                                       "(profiles/moe_gemm_k3_e64_t8.md), scaled to this launch by its algorithmic "
+                                       "bytes (active experts)",
                      "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_avg, 5),
                      "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"},
         "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),
