@@ -285,6 +285,73 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ sweep
+def run_sweep(args):
+    """Token-count sweep on one GPU: the K3 layer of the sweep workload (seed 4,
+    uniform bias) built once, one JSON line per T with tokens/s, the layer's
+    HBM-roofline fraction, its FLOP rate against the bf16 tensor peak (the hi/lo
+    E4M3 activations make the routed MMAs cost what bf16 would), the expert
+    kernels' GB/s and the per-stage times."""
+    import torch
+    from lmoe_inputs import configs as C
+    from lmoe_inputs import generate as G
+    from latent_mixture_experts_gb300 import LatentMoE, build
+    build.build()
+    torch.cuda.set_device(0)
+    Ts = [int(t) for t in args.sweep.split(",")]
+    wl = C.workload("k3_sweep_t1")
+    cfg = wl.cfg
+    W = G.gen_weights(wl, device="cuda")
+    layer = LatentMoE(cfg, W, max_tokens=max(Ts))
+    pk = peaks()
+    flops_per_token = 1_436_811_264
+    for T in Ts:
+        wlT = replace(wl, T=T, name=f"k3_sweep_t{T}")
+        xs = [G.gen_x(replace(wlT, seed=wl.seed + 7919 * (i + 1)), device="cuda") for i in range(4)]
+        out = torch.empty(T, cfg.d_model, dtype=torch.bfloat16, device="cuda")
+        U = []
+        for xb in xs:
+            layer.lmoe_forward(xb, out=out)
+            U.append(layer.lmoe_last_active_experts())
+        for i in range(max(args.warmup, 3)):
+            layer.lmoe_forward(xs[i % 4], out=out)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        layer.lmoe_forward(xs[0], out=out)
+        torch.cuda.synchronize()
+        est = time.perf_counter() - t0
+        steps = max(10, min(args.steps, int(0.5 / max(est, 1e-5))))
+        layer.lmoe_set_profiling(steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            layer.lmoe_forward(xs[i % 4], out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        prof = layer.lmoe_profile_get()
+        layer.lmoe_set_profiling(0)
+        layer.lmoe_sync_status()
+        U_mean = sum(U[i % 4] for i in range(steps)) / steps
+        layer_bytes = DENSE_BYTES + U_mean * EXPERT_BYTES + T * TOKEN_IO_BYTES
+        din, F, k = cfg.d_latent, cfg.d_expert_ff, cfg.top_k
+        gu_bytes = U_mean * 2 * (F * din // 2 + F * din // 32)
+        dn_bytes = U_mean * (din * F // 2 + din * F // 32)
+        gu = prof["expert_gate_up"][0] / max(prof["expert_gate_up"][1], 1)
+        dn = prof["expert_down"][0] / max(prof["expert_down"][1], 1)
+        tflops = T * flops_per_token / (ms * 1e-3) / 1e12
+        print(json.dumps({
+            "workload": wlT.name, "T": T, "steps": steps, "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "ms_per_step": round(ms, 4), "active_experts_mean": round(U_mean, 1),
+            "layer_hbm": {"bytes": int(layer_bytes), "gbs": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+                          "frac": round(layer_bytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)},
+            "layer_tensor": {"tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / pk["bf16"], 4)},
+            "expert_gate_up_gbs": round(gu_bytes / (gu * 1e-3) / 1e9, 1),
+            "expert_down_gbs": round(dn_bytes / (dn * 1e-3) / 1e9, 1),
+            "stage_ms": {n: round(v[0] / max(v[1], 1), 4) for n, v in prof.items()}}), flush=True)
+    layer.close()
+
+
 # ------------------------------------------------------------- reference
 def run_reference(args):
     """The fp64 oracle as the reference arm, on the host cores.  One step is
@@ -388,10 +455,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=2)
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated token counts: one JSON line per T on one GPU (not the driver's contract)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

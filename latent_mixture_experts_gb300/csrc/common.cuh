@@ -25,6 +25,20 @@ __device__ __forceinline__ float glu_act(float g, float u, int act, float b1, fl
   return a * ub;
 }
 
+// Hardware approximations for the expert epilogues, whose output is encoded
+// as two E4M3 terms right after (relative error ~2^-11, below that encoding).
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float glu_act_fast(float g, float u, int act, float b1, float b2) {
+  const float sg = sigmoid_fast(g);
+  if (act == 1) return g * sg * u;
+  return b1 * tanh_fast(g * (1.0f / b1)) * sg * (b2 * tanh_fast(u * (1.0f / b2)));
+}
+
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
 }

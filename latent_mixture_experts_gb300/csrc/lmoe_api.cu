@@ -81,7 +81,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int dense_bn(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
-int moe_bn(int T, int k, int E) { return static_cast<long long>(T) * k <= 4LL * E ? 16 : 64; }
+int moe_bn(int T, int k, int E) { return moe_tile_tokens(static_cast<long long>(T) * k, E); }
 
 // K splits of a dense GEMM: fill about one wave of CTAs, at least two
 // 64-wide k-blocks per split.
@@ -521,6 +521,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.sfa_up = h->sfa_up;
     p.sfb = h->xsf;
     p.tiles = h->tiles;
+    p.tile_off = h->tile_off;
     p.ntiles = h->ntiles;
     p.perm = h->perm;
     p.G = h->G;

@@ -72,11 +72,18 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
 // tcgen05 staging image, per BN-row tile and 128-wide k-group.
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
                                 uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+// Same from bf16 token rows (layers whose experts take x itself).
+cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
+                                     uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 
 // Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
 // 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
 // prefill keep 128-row items so two accumulators fit tensor memory.
 __host__ __device__ constexpr int moe_rows_per_item(int BN) { return BN >= 64 ? 128 : 256; }
+// Token tile of the grouped expert GEMMs from the mean assignments per expert.
+inline int moe_tile_tokens(long long assignments, int n_experts) {
+  return assignments <= 4LL * n_experts ? 16 : assignments <= 16LL * n_experts ? 32 : 64;
+}
 
 struct MoeGemmParams {
   CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp] (boxes of moe_rows_per_item rows);
@@ -85,6 +92,7 @@ struct MoeGemmParams {
   const uint8_t* sfa_up;
   const uint8_t* sfb;            // activation scale atoms [Ppad/BN][G][NA][512]
   const int4* tiles;
+  const int32_t* tile_off;       // [E+1] padded row offsets (multiples of BN)
   const int32_t* ntiles;
   const int32_t* perm;
   const float* G;                // [T*k] routing weights (down pass)
@@ -101,9 +109,17 @@ struct MoeGemmParams {
   float b1, b2;
   // down epilogue
   float* y;                      // [T*k][din] fp32, G-scaled expert outputs
+  // FP8 weights: fp32 scale per 128 x 128 block, [E][NB][KB]; wsc1 = up scales (gate/up pass)
+  const float* wsc0;
+  const float* wsc1;
+  int NB, KB;
 };
 cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
 cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+// FP8 E4M3 weights with 128 x 128 fp32 block scales (BN 16 or 32).
+cudaError_t launch_moe_fp8_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+cudaError_t launch_moe_fp8_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+cudaError_t launch_dequant_fp8_block128(const uint8_t* q, const float* s, int N, int K, void* out, cudaStream_t st);
 
 // u[t] = sum_j y[t*k + j] (slot order); u_hat = w * u / sqrt(mean(u^2) + eps) -> bf16.
 cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,

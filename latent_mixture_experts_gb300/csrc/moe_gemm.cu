@@ -22,13 +22,11 @@
 //     weighted sum is finished by the combine kernel in slot order).
 #include "common.cuh"
 #include "lmoe_internal.h"
+#include "moe_common.cuh"
 
 namespace lmoe {
 
 namespace {
-
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int BN, bool GU>
 struct MoeCfg {
@@ -58,13 +56,6 @@ struct MoeCfg {
   static_assert(kTmemUsed <= 512, "tensor memory budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
 
 template <int BN, bool GU>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
@@ -114,8 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const int4 tile = p.tiles[w / p.MT];
-        const int mt = w % p.MT;
+        int mt;
+        const int4 tile = decode_item<BN>(p, w, mt);
         const int e = tile.x, row0 = tile.y;
         // second box: the up rows of the same features, or the next RB down rows
         const int arow = e * p.N_out + mt * C::IR;
@@ -193,9 +184,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint32_t use = titer / C::kAccBufs;
       if (!mbar_wait(&acc_full[b], use & 1, p.err, kErrTimeout)) break;
       tc_fence_after();
-      const int4 tile = p.tiles[w / p.MT];
-      const int mt = w % p.MT;
+      int mt;
+      const int4 tile = decode_item<BN>(p, w, mt);
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
+      // down pass: assignment and routing weight of the tile's rows j = lane, lane + 32
+      int a_lo = 0, a_hi = 0;
+      float g_lo = 0.f, g_hi = 0.f;
+      if (!GU) {
+        if (lane < nrows) {
+          a_lo = p.perm[p0 + lane];
+          g_lo = p.G[a_lo];
+        }
+        if (BN > 32 && lane + 32 < nrows) {
+          a_hi = p.perm[p0 + lane + 32];
+          g_hi = p.G[a_hi];
+        }
+      }
       const uint32_t acc_base = tbase + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAcc;
 #pragma unroll 1
       for (int t = 0; t < (GU ? C::kTiles : C::kNAcc); ++t) {
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               if (j >= nrows) continue;                      // warp-uniform
               const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
               const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
-              const float h = f_ok ? glu_act(gv, uv, p.act, p.b1, p.b2) : 0.0f;
+              const float h = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
               const HiLo e = quant_hilo_warp(h);
               const size_t r = static_cast<size_t>(row0) + j;
               p.hq[(2 * r) * p.Fp + f] = e.q_hi;
@@ -243,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             for (int jj = 0; jj < 16; ++jj) {
               const int j = j0 + jj;
               if (j >= nrows) continue;
-              const int a = p.perm[p0 + j];
-              const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * p.G[a];
+              const int a = __shfl_sync(0xFFFFFFFFu, j < 32 ? a_lo : a_hi, j & 31);
+              const float gw = __shfl_sync(0xFFFFFFFFu, j < 32 ? g_lo : g_hi, j & 31);
+              const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
               if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
             }
           }
@@ -274,7 +279,8 @@ cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
 // computed once and written to the padded rows 2r, 2r+1 of each of the
 // token's k assignments; their scales go into the staging image of each
 // row's tile.
-__global__ void quant_gather_kernel(const float* __restrict__ xc, int T, int k, int din, int Kp,
+template <typename TIn>
+__global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, uint8_t* __restrict__ xq,
                                     uint8_t* __restrict__ xsf) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -282,7 +288,7 @@ __global__ void quant_gather_kernel(const float* __restrict__ xc, int T, int k, 
   if (gw >= T * nblk) return;
   const int t = gw / nblk, blk = gw % nblk;
   const int c = blk * 32 + lane;
-  const float v = c < din ? xc[static_cast<size_t>(t) * din + c] : 0.0f;
+  const float v = c < din ? static_cast<float>(xc[static_cast<size_t>(t) * din + c]) : 0.0f;
   const HiLo e = quant_hilo_warp(v);
   const int NA = (2 * BN + 127) / 128;
   const int KG = Kp / 128;
@@ -396,6 +402,7 @@ int ew_grid(size_t n) {
 cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s) {
   switch (BN) {
     case 16: return launch_moe<16, true>(p, grid, s);
+    case 32: return launch_moe<32, true>(p, grid, s);
     case 64: return launch_moe<64, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
@@ -403,6 +410,7 @@ cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStr
 cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s) {
   switch (BN) {
     case 16: return launch_moe<16, false>(p, grid, s);
+    case 32: return launch_moe<32, false>(p, grid, s);
     case 64: return launch_moe<64, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
@@ -413,8 +421,19 @@ cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, 
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 32);
-  quant_gather_kernel<<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block), 32 * warps_per_block,
-                        0, s>>>(xc, T, k, din, Kp, inv_pad, BN, xq, xsf);
+  quant_gather_kernel<float><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
+                               32 * warps_per_block, 0, s>>>(xc, T, k, din, Kp, inv_pad, BN, xq, xsf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
+                                     uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const long long warps = static_cast<long long>(T) * (Kp / 32);
+  quant_gather_kernel<__nv_bfloat16><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
+                                       32 * warps_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, k, din,
+                                                                    Kp, inv_pad, BN, xq, xsf);
   return cudaGetLastError();
 }
 
