@@ -122,8 +122,9 @@ typedef struct lmoe_ctx* lmoe_handle;
  * encode the TMA descriptors of the weights.  Synchronises `stream`.
  * Errors: INVALID_ARG (null pointers, bad shapes), UNSUPPORTED (shapes the
  * kernels do not cover: d, l, F, Fs must be multiples of 32; E <= 2048;
- * k <= 32; MXFP4 latent layers only in this build; the current device is
- * not an sm_103 GPU), OOM, CUDA.  On error *out is NULL. */
+ * k <= 32; MXFP4 experts need a latent layer, FP8 block-128 experts a
+ * non-latent one without the norm and with d, F, Fs multiples of 128; the
+ * current device is not an sm_103 GPU), OOM, CUDA.  On error *out is NULL. */
 LMOE_API lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStream_t stream, lmoe_handle* out);
 
 /* Router only (Kimi K3 card, router steps; port notes item 3): topk_idx
@@ -180,7 +181,8 @@ LMOE_API lmoe_status lmoe_dispatch_noalloc(const int32_t* topk_idx, int T, int k
 
 /* Copy an intermediate of the last lmoe_forward on this handle out of the
  * workspace (stream-ordered): "logits" fp32 [T][E] (router z), "xc" fp32
- * [T][l], "u" fp32 [T][l] (expert sum), "u_hat" bf16 [T][l], "h_shared"
+ * [T][l], "u" fp32 [T][l] (expert sum; [T][d] for non-latent layers, where
+ * it is y_routed), "u_hat" bf16 [T][l] (latent layers), "h_shared"
  * bf16 [T][Fs], "counts" int32 [E], "offsets" int32 [E+1], "perm" int32
  * [T*k].  `bytes` must equal the tensor's size for the last T. */
 LMOE_API lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t stream);

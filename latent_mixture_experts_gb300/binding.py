@@ -197,8 +197,9 @@ class LatentMoE:
 
     def lmoe_debug_tensor(self, name: str, T: int, stream=None):
         c = self.cfg
+        dx = c.d_latent or c.d_model          # width of the expert sum (the latent, or d for K2-style layers)
         shapes = {"logits": ((T, c.n_experts), torch.float32), "xc": ((T, c.d_latent), torch.float32),
-                  "u": ((T, c.d_latent), torch.float32), "u_hat": ((T, c.d_latent), torch.bfloat16),
+                  "u": ((T, dx), torch.float32), "u_hat": ((T, dx), torch.bfloat16),
                   "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "counts": ((c.n_experts,), torch.int32),
                   "offsets": ((c.n_experts + 1,), torch.int32), "perm": ((T * c.top_k,), torch.int32)}
         shape, dt = shapes[name]

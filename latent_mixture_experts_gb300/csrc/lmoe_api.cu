@@ -28,6 +28,9 @@ struct lmoe_ctx {
   lmoe_weights w;
   int dev = 0, num_sms = 148;
   int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
+  int dx = 0;          // width the routed experts read and write: the latent, or d for non-latent layers
+  bool fp8 = false;    // experts in FP8 E4M3 with 128 x 128 fp32 block scales
+  void *sh_g16 = nullptr, *sh_u16 = nullptr, *sh_d16 = nullptr;   // bf16 copies of an FP8 shared expert
   int Kp = 0, Fp = 0, MT_gu = 0, MT_dn = 0, KG_gu = 0, KG_dn = 0, MTa_gu = 0, MTa_dn = 0;
   int Tm = 0, Pm = 0, Ppad = 0, max_tiles = 0, nchunks_max = 0;
   // device memory
@@ -231,7 +234,11 @@ lmoe_status validate_cfg(const lmoe_config* c) {
     return LMOE_ERR_INVALID_ARG;
   if (c->act != LMOE_ACT_SITU && c->act != LMOE_ACT_SWIGLU) return LMOE_ERR_INVALID_ARG;
   if (c->expert_wfmt != LMOE_W_MXFP4 && c->expert_wfmt != LMOE_W_FP8_BLOCK128) return LMOE_ERR_INVALID_ARG;
-  if (c->expert_wfmt != LMOE_W_MXFP4 || c->d_latent == 0) return LMOE_ERR_UNSUPPORTED;
+  // MXFP4 experts: latent layers (Kimi K3); FP8 block-128 experts: non-latent layers (Kimi K2)
+  if (c->expert_wfmt == LMOE_W_MXFP4 && c->d_latent == 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->expert_wfmt == LMOE_W_FP8_BLOCK128 &&
+      (c->d_latent != 0 || c->use_latent_norm || c->d_model % 128 || c->d_expert_ff % 128 || c->d_shared_ff % 128))
+    return LMOE_ERR_UNSUPPORTED;
   if (c->d_model % 32 || c->d_latent % 32 || c->d_expert_ff % 32 || c->d_shared_ff % 32) return LMOE_ERR_UNSUPPORTED;
   if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->max_tokens) * c->top_k > (1LL << 30)) return LMOE_ERR_UNSUPPORTED;
@@ -240,9 +247,14 @@ lmoe_status validate_cfg(const lmoe_config* c) {
 }
 
 lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
-  const void* need16[] = {w->router_w, w->router_bias, w->w_down_latent, w->w_up_latent};
+  const void* need16[] = {w->router_w, w->router_bias};
   for (const void* p : need16)
     if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+  if (c->d_latent) {
+    const void* lat[] = {w->w_down_latent, w->w_up_latent};
+    for (const void* p : lat)
+      if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+  }
   if (c->use_latent_norm && (!w->norm_w || !aligned(w->norm_w, 16))) return LMOE_ERR_INVALID_ARG;
   const void* need32[] = {w->ex_gate_q, w->ex_up_q, w->ex_down_q, w->ex_gate_s, w->ex_up_s, w->ex_down_s};
   for (const void* p : need32)
@@ -251,6 +263,11 @@ lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
     const void* sh[] = {w->sh_gate, w->sh_up, w->sh_down};
     for (const void* p : sh)
       if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+    if (c->expert_wfmt == LMOE_W_FP8_BLOCK128) {
+      const void* shs[] = {w->sh_gate_s, w->sh_up_s, w->sh_down_s};
+      for (const void* p : shs)
+        if (!p || !aligned(p, 16)) return LMOE_ERR_INVALID_ARG;
+    }
   }
   return LMOE_OK;
 }
@@ -299,10 +316,12 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->k = cfg->top_k;
   h->F = cfg->d_expert_ff;
   h->Fs = cfg->d_shared_ff;
-  h->Kp = static_cast<int>(align_up(h->din, 128));
+  h->dx = h->din ? h->din : h->d;
+  h->fp8 = cfg->expert_wfmt == LMOE_W_FP8_BLOCK128;
+  h->Kp = static_cast<int>(align_up(h->dx, 128));
   h->Fp = static_cast<int>(align_up(h->F, 128));
   h->MT_gu = h->Fp / 128;
-  h->MT_dn = ceil_div(h->din, 128);
+  h->MT_dn = ceil_div(h->dx, 128);
   h->MTa_gu = (h->MT_gu + 1) / 2 * 2;
   h->MTa_dn = (h->MT_dn + 3) / 4 * 4;   // the down pass copies the atoms of up to four 128-row tiles per stage
   h->KG_gu = h->Kp / 128;
@@ -328,7 +347,10 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   }
   const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
   const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
-  const bool pad_gu = h->Kp != h->din, pad_dn = h->Fp != h->F;
+  const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
+  const size_t sfa_gu_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512;
+  const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512;
+  const bool sh16 = h->fp8 && h->Fs;
 
   auto carve = [&](char* base) {
     Carve c;
@@ -350,15 +372,20 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->xsf = c.take<uint8_t>(xsf_bytes, base);
     h->hq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Fp, base);
     h->hsf = c.take<uint8_t>(hsf_bytes, base);
-    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->din, base);
-    h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->din, base);
-    h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->din, base);
+    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->dx, base);
+    h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->dx, base);
+    h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);
     h->x_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
     h->out_stage = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->d, base);
-    h->sfa_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512, base);
-    h->sfa_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512, base);
-    h->sfa_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512, base);
+    h->sfa_gate = c.take<uint8_t>(sfa_gu_bytes, base);
+    h->sfa_up = c.take<uint8_t>(sfa_gu_bytes, base);
+    h->sfa_down = c.take<uint8_t>(sfa_dn_bytes, base);
+    if (sh16) {
+      h->sh_g16 = c.take<uint16_t>(static_cast<size_t>(h->Fs) * h->d, base);
+      h->sh_u16 = c.take<uint16_t>(static_cast<size_t>(h->Fs) * h->d, base);
+      h->sh_d16 = c.take<uint16_t>(static_cast<size_t>(h->d) * h->Fs, base);
+    }
     if (pad_gu) {
       h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
       h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
@@ -384,9 +411,19 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const uint8_t* sg = static_cast<const uint8_t*>(w->ex_gate_s);
   const uint8_t* su = static_cast<const uint8_t*>(w->ex_up_s);
   const uint8_t* sd = static_cast<const uint8_t*>(w->ex_down_s);
-  if (launch_relayout_sfa(sg, h->E, h->F, h->din / 32, h->MTa_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
-      launch_relayout_sfa(su, h->E, h->F, h->din / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
-      launch_relayout_sfa(sd, h->E, h->din, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess)
+  if (!h->fp8 &&
+      (launch_relayout_sfa(sg, h->E, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
+       launch_relayout_sfa(su, h->E, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
+       launch_relayout_sfa(sd, h->E, h->dx, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess))
+    return fail(LMOE_ERR_CUDA);
+  // FP8 shared expert: one bf16 copy at create (0.26% of a K2 layer's bytes), then the bf16 GEMMs
+  if (sh16 &&
+      (launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_gate), static_cast<const float*>(w->sh_gate_s),
+                                   h->Fs, h->d, h->sh_g16, stream) != cudaSuccess ||
+       launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_up), static_cast<const float*>(w->sh_up_s),
+                                   h->Fs, h->d, h->sh_u16, stream) != cudaSuccess ||
+       launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_down), static_cast<const float*>(w->sh_down_s),
+                                   h->d, h->Fs, h->sh_d16, stream) != cudaSuccess))
     return fail(LMOE_ERR_CUDA);
   h->codes_gate = w->ex_gate_q;
   h->codes_up = w->ex_up_q;
@@ -405,18 +442,26 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   }
   bool ok = true;
   ok &= map_bf16(&h->m_router, w->router_w, h->d, h->E, 128);
-  ok &= map_bf16(&h->m_wdown, w->w_down_latent, h->d, h->din, 128);
-  ok &= map_bf16(&h->m_wup, w->w_up_latent, h->din, h->d, 128);
+  if (h->din) {
+    ok &= map_bf16(&h->m_wdown, w->w_down_latent, h->d, h->din, 128);
+    ok &= map_bf16(&h->m_wup, w->w_up_latent, h->din, h->d, 128);
+  }
   if (h->Fs) {
-    ok &= map_bf16(&h->m_shg, w->sh_gate, h->d, h->Fs, 128);
-    ok &= map_bf16(&h->m_shu, w->sh_up, h->d, h->Fs, 128);
-    ok &= map_bf16(&h->m_shd, w->sh_down, h->Fs, h->d, 128);
+    ok &= map_bf16(&h->m_shg, sh16 ? h->sh_g16 : w->sh_gate, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shu, sh16 ? h->sh_u16 : w->sh_up, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shd, sh16 ? h->sh_d16 : w->sh_down, h->Fs, h->d, 128);
   }
   for (int i = 0; i < 2; ++i) {
     const int rows = 128 << i;
-    ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-    ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-    ok &= map_fp4(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->din, rows);
+    if (h->fp8) {
+      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->dx, rows);
+    } else {
+      ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_fp4(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->dx, rows);
+    }
   }
   if (!ok) return fail(LMOE_ERR_CUDA);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
@@ -463,7 +508,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   if (T == 0) return LMOE_OK;
   if (!x || !out || !aligned(x, 16) || !aligned(out, 16) || x == out) return LMOE_ERR_INVALID_ARG;
   int launches = 0;
-  const int d = h->d, din = h->din, Fs = h->Fs;
+  const int d = h->d, din = h->din, dx = h->dx, Fs = h->Fs;
   const int BN = dense_bn(T);
   const int nt = ceil_div(T, BN);
   const int nkb_d = ceil_div(d, 64);
@@ -472,12 +517,12 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   lmoe_status s = run_router(h, x, T, st, launches);
   if (s != LMOE_OK) return s;
   // 3 dispatch
-  const int BNm = moe_bn(T, h->k, h->E);
+  const int BNm = h->fp8 ? std::min(moe_bn(T, h->k, h->E), 32) : moe_bn(T, h->k, h->E);
   s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
   if (s != LMOE_OK) return s;
 
-  // 4 latent down-projection
-  {
+  // 4 latent down-projection (latent layers only)
+  if (din) {
     StageTimer tm(h, LMOE_STAGE_LATENT_DOWN, st);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
@@ -504,7 +549,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   // 5 activations -> hi/lo E4M3 in expert-tile order
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
-    LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+    if (din)
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+    else
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
     ++launches;
     tm.done();
   }
@@ -512,7 +560,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
-    const int RB = moe_rows_per_item(BNm);
+    const int RB = h->fp8 ? fp8_rows_per_item(BNm) : moe_rows_per_item(BNm);
     const int mi = RB == 256 ? 1 : 0;
     p.a_gate = h->m_exg[mi];
     p.a_up = h->m_exu[mi];
@@ -537,8 +585,12 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.b1 = h->cfg.situ_beta;
     p.b2 = h->cfg.situ_linear_beta;
     p.y = h->y;
+    p.wsc0 = static_cast<const float*>(h->w.ex_gate_s);
+    p.wsc1 = static_cast<const float*>(h->w.ex_up_s);
+    p.NB = ceil_div(h->F, 128);
+    p.KB = ceil_div(dx, 128);
     StageTimer tgu(h, LMOE_STAGE_EXPERT_GU, st);
-    LMOE_TRY(launch_moe_gate_up(p, BNm, h->num_sms, st));
+    LMOE_TRY(h->fp8 ? launch_moe_fp8_gate_up(p, BNm, h->num_sms, st) : launch_moe_gate_up(p, BNm, h->num_sms, st));
     ++launches;
     tgu.done();
     MoeGemmParams q = p;
@@ -547,20 +599,24 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.sfa_gate = h->sfa_down;
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
-    q.N_out = din;
-    q.MT = ceil_div(din, 2 * RB);
+    q.N_out = dx;
+    q.MT = ceil_div(dx, 2 * RB);
     q.MTa = h->MTa_dn;
     q.KG = h->KG_dn;
+    q.wsc0 = static_cast<const float*>(h->w.ex_down_s);
+    q.wsc1 = nullptr;
+    q.NB = ceil_div(dx, 128);
+    q.KB = ceil_div(h->F, 128);
     StageTimer tdn(h, LMOE_STAGE_EXPERT_DOWN, st);
-    LMOE_TRY(launch_moe_down(q, BNm, h->num_sms, st));
+    LMOE_TRY(h->fp8 ? launch_moe_fp8_down(q, BNm, h->num_sms, st) : launch_moe_down(q, BNm, h->num_sms, st));
     ++launches;
     tdn.done();
   }
   // 8 expert sum in slot order + latent RMSNorm
   {
     StageTimer tm(h, LMOE_STAGE_COMBINE, st);
-    LMOE_TRY(launch_combine_norm(h->y, T, h->k, din, h->w.norm_w, h->cfg.use_latent_norm, h->cfg.norm_eps, h->u,
-                                 h->u_hat, st));
+    LMOE_TRY(launch_combine_norm(h->y, T, h->k, dx, h->w.norm_w, din && h->cfg.use_latent_norm, h->cfg.norm_eps,
+                                 h->u, h->u_hat, st));
     ++launches;
     tm.done();
   }
@@ -591,7 +647,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     tm.done();
   }
   // 10 Delta = u_hat W_up^T + h_shared W_shared_down^T
-  {
+  if (din) {
     StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
@@ -616,6 +672,32 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
     LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
     launches += 2;
+    tm.done();
+  } else {
+    // non-latent layer (Kimi K2 card): Delta = sum_i G_i E_i + h_shared W_shared_down^T
+    StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
+    int splits = 0;
+    if (Fs) {
+      DenseParams p;
+      std::memset(&p, 0, sizeof(p));
+      p.a0 = h->m_shd;
+      if (!map_bf16(&p.b0, h->h_s, Fs, T, BN)) return LMOE_ERR_CUDA;
+      p.mode = 0;
+      p.nkb0 = ceil_div(Fs, 64);
+      p.nkb = p.nkb0;
+      p.M0 = d;
+      p.mtiles0 = ceil_div(d, 128);
+      p.T = T;
+      p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
+      p.ldo = d;
+      p.out = h->part;
+      p.err = h->err;
+      LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+      ++launches;
+      splits = p.splits;
+    }
+    LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, st));
+    ++launches;
     tm.done();
   }
   const size_t n = static_cast<size_t>(T) * h->k;
@@ -652,10 +734,10 @@ lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t
     want = T * h->din * 4;
   } else if (!std::strcmp(name, "u")) {
     src = h->u;
-    want = T * h->din * 4;
+    want = T * h->dx * 4;
   } else if (!std::strcmp(name, "u_hat")) {
     src = h->u_hat;
-    want = T * h->din * 2;
+    want = T * h->dx * 2;
   } else if (!std::strcmp(name, "h_shared")) {
     src = h->h_s;
     want = T * h->Fs * 2;

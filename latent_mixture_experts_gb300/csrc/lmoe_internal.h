@@ -80,6 +80,8 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
 // 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
 // prefill keep 128-row items so two accumulators fit tensor memory.
 __host__ __device__ constexpr int moe_rows_per_item(int BN) { return BN >= 64 ? 128 : 256; }
+// Weight rows per TMA box of the FP8-weight expert GEMMs.
+__host__ __device__ constexpr int fp8_rows_per_item(int BN) { return BN <= 16 ? 256 : 128; }
 // Token tile of the grouped expert GEMMs from the mean assignments per expert.
 inline int moe_tile_tokens(long long assignments, int n_experts) {
   return assignments <= 4LL * n_experts ? 16 : assignments <= 16LL * n_experts ? 32 : 64;

@@ -20,7 +20,7 @@ namespace {
 template <int BN, bool GU>
 struct Fp8Cfg {
   static constexpr int N = 2 * BN;                   // hi/lo columns of BN assignments
-  static constexpr int RB = BN <= 16 ? 256 : 128;    // weight rows per TMA box
+  static constexpr int RB = fp8_rows_per_item(BN);   // weight rows per TMA box
   static constexpr int kTiles = RB / 128;
   static constexpr int kBoxes = 2;                   // gate + up, or two down boxes
   static constexpr int IR = GU ? RB : 2 * RB;        // weight rows of one work item
