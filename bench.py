@@ -38,13 +38,45 @@ sys.path.insert(0, ROOT)
 
 METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
 UNIT = "tokens/s"
-EXPERT_BYTES = 17_547_264          # one K3 expert: 3 x 3584 x 3072 E2M1 codes + E8M0 scales
-DENSE_BYTES = 379_857_408          # K3 bf16 router, W_down, W_up, norm, shared MLP + fp32 bias
-TOKEN_IO_BYTES = 28_672            # x in + Delta out, bf16, per token
-# DRAM bytes per algorithmic byte of the gate/up expert kernel, from one ncu
-# capture of the current kernel (read + write 702.2 MB for 645 MB algorithmic).
-# Set to None when the kernel changes until it is captured again.
-GU_DRAM_PER_ALGO_BYTE = 1.089
+# DRAM bytes per algorithmic byte of the K3 gate/up expert kernel, from one
+# ncu capture of the kernel as it stands (profiles/moe_gemm_k3_e64_t8.md).
+# None when the kernel has changed since the counters were taken.
+GU_DRAM_PER_ALGO_BYTE = None
+
+
+def _mat_bytes(cfg, N: int, K: int) -> int:
+    """Stored bytes of one N x K weight matrix in the expert format: MXFP4
+    (two E2M1 codes per byte + one E8M0 per 32) or FP8 E4M3 with an fp32
+    scale per 128 x 128 block."""
+    if cfg.expert_wfmt == "mxfp4":
+        return N * K // 2 + N * K // 32
+    return N * K + 4 * (-(-N // 128)) * (-(-K // 128))
+
+
+def accounting(cfg) -> dict:
+    """Algorithmic bytes and FLOPs of the layer (each weight byte read once,
+    activations between kernels in the format the path stores them).
+
+    expert: weight bytes of one routed expert (gate + up + down);
+    dense: router (bf16 + fp32 bias), latent projections and norm (bf16),
+    shared MLP (bf16 for K3, FP8 block-128 as stored for K2);
+    token_io: x in + Delta out (bf16); flops_per_token: 2 x MACs of every
+    contraction (router, latent, k experts, shared)."""
+    d, l, E, k, F, Fs = cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k, cfg.d_expert_ff, cfg.d_shared_ff
+    din = l or d
+    gu_w = 2 * _mat_bytes(cfg, F, din)
+    dn_w = _mat_bytes(cfg, din, F)
+    dense = E * d * 2 + E * 4
+    if l:
+        dense += 2 * l * d * 2 + (l * 2 if cfg.use_latent_norm else 0)
+    if Fs:
+        dense += 3 * Fs * d * 2 if cfg.expert_wfmt == "mxfp4" else 2 * _mat_bytes(cfg, Fs, d) + _mat_bytes(cfg, d, Fs)
+    flops = 2 * E * d + (4 * l * d if l else 0) + k * 6 * F * din + 6 * Fs * d
+    # hi/lo E4M3 activation pairs with one E8M0 per 32 in, the same for h
+    act_in = 2 * din + 2 * din // 32
+    h_io = 2 * F + 2 * F // 32
+    return dict(din=din, gu_w=gu_w, dn_w=dn_w, expert=gu_w + dn_w, dense=dense, token_io=2 * d * 2,
+                flops_per_token=flops, gu_per_assign=act_in + h_io, dn_per_assign=h_io + din * 4)
 
 
 def peaks():
@@ -127,8 +159,12 @@ def cpu_baseline(wl, W_dev, x_dev, ntok=2) -> dict:
     O, Wn = oracle_for(wl, W_dev)
     xb = x_dev[:ntok].cpu().view(torch.int16).numpy().view(np.uint16)
     layer = O.Layer(wl.cfg, Wn)
-    for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w", "sh_gate", "sh_up", "sh_down"):
-        layer.dense(name)            # host-side fp64 copies of the dense weights: input preparation
+    for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w"):
+        if name in Wn:
+            layer.dense(name)        # host-side fp64 copies of the dense weights: input preparation
+    for name in ("sh_gate", "sh_up", "sh_down"):
+        if name in Wn:
+            layer.shared(name)
     t0 = time.perf_counter()
     O.forward(layer, xb)
     dt = time.perf_counter() - t0
@@ -212,19 +248,20 @@ def run_ours(args):
     U_mean = sum(U[i % 4] for i in range(steps)) / steps
     pk = peaks()
 
-    # dominant kernel: grouped MXFP4 gate/up GEMM.  Algorithmic bytes per
-    # launch: the selected experts' gate+up codes and scales, the hi/lo E4M3
-    # activations in (with their scales) and the hi/lo h out.
-    din, F, k = cfg.d_latent, cfg.d_expert_ff, cfg.top_k
-    gu_w = 2 * (F * din // 2 + F * din // 32)
-    gu_bytes = U_mean * gu_w + T * k * (2 * din + 2 * din // 32) + T * k * (2 * F + 2 * F // 32)
+    # dominant kernel: the grouped gate/up expert GEMM.  Algorithmic bytes
+    # per launch: the selected experts' gate+up weights (codes and scales),
+    # the hi/lo E4M3 activations in (with their scales) and the hi/lo h out.
+    A = accounting(cfg)
+    din, F, k = A["din"], cfg.d_expert_ff, cfg.top_k
+    gu_bytes = U_mean * A["gu_w"] + T * k * A["gu_per_assign"]
     gu_ms, gu_n = prof["expert_gate_up"]
     gu_avg = gu_ms / max(gu_n, 1)
     achieved = gu_bytes / (gu_avg * 1e-3) / 1e9
-    dn_w = din * F // 2 + din * F // 32
-    dn_bytes = U_mean * dn_w + T * k * (2 * F + 2 * F // 32) + T * k * din * 4
+    dn_bytes = U_mean * A["dn_w"] + T * k * A["dn_per_assign"]
     dn_ms, dn_n = prof["expert_down"]
-    layer_bytes = DENSE_BYTES + U_mean * EXPERT_BYTES + T * TOKEN_IO_BYTES
+    layer_bytes = A["dense"] + U_mean * A["expert"] + T * A["token_io"]
+    fp4 = cfg.expert_wfmt == "mxfp4"
+    gu_traffic = GU_DRAM_PER_ALGO_BYTE if fp4 else None
     stages = {name: round(v[0] / max(v[1], 1), 5) for name, v in prof.items()}
 
     # end to end through the host-buffer entry point
@@ -251,17 +288,21 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1 x e4m3(hi+lo) block-scaled; bf16 dense; fp32 accumulate",
-        "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to MXFP4; x ~ N(0,1) bf16)",
-        "config": {"workload": wl.name, "T": T, "d_model": cfg.d_model, "d_latent": din, "n_experts": cfg.n_experts,
+        "vs_baseline": None,
+        "dtype": ("e2m1 x e4m3(hi+lo) block-scaled; bf16 dense; fp32 accumulate" if fp4 else
+                  "e4m3 x e4m3(hi+lo), fp32 block-128 scales; bf16 dense; fp32 accumulate"),
+        "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to "
+                + ("MXFP4" if fp4 else "FP8 E4M3 block-128") + "; x ~ N(0,1) bf16)",
+        "config": {"workload": wl.name, "T": T, "d_model": cfg.d_model, "d_latent": cfg.d_latent, "n_experts": cfg.n_experts,
                    "top_k": k, "d_expert_ff": F, "d_shared_ff": cfg.d_shared_ff, "expert_format": cfg.expert_wfmt,
                    "parallelism": f"replicas x{world}", "token_batches_rotated": 4,
                    "l2": "no flush: each step streams the selected experts' weights (GBs) >> 129 MB L2",
                    "active_experts_mean": round(U_mean, 1)},
-        "roofline": {"kernel": "moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+        "roofline": {"kernel": ("moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)" if fp4 else
+                                "moe_fp8_kernel<gate/up> (grouped E4M3 x E4M3 hi/lo, block-128 promotion, tcgen05)"),
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm"], 4),
-                     "traffic": int(GU_DRAM_PER_ALGO_BYTE * gu_bytes) if GU_DRAM_PER_ALGO_BYTE else None,
+                     "traffic": int(gu_traffic * gu_bytes) if gu_traffic else None,
                      "traffic_source": "ncu dram__bytes_read+write of this kernel on the 64-expert K3-shaped case "
                                        "(profiles/moe_gemm_k3_e64_t8.md), scaled to this launch by its algorithmic "
                                        "bytes (active experts)",
@@ -269,7 +310,10 @@ def run_ours(args):
                      "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"},
         "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),
                            "achieved": round(layer_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": pk["hbm"],
-                           "unit": "GB/s", "frac": round(layer_bytes / (ms_step * 1e-3) / 1e9 / pk["hbm"], 4)},
+                           "unit": "GB/s", "frac": round(layer_bytes / (ms_step * 1e-3) / 1e9 / pk["hbm"], 4),
+                           "tflops": round(T * A["flops_per_token"] / (ms_step * 1e-3) / 1e12, 1),
+                           "frac_of_bf16_peak": round(T * A["flops_per_token"] / (ms_step * 1e-3) / 1e12
+                                                      / pk["bf16"], 4)},
         "down_kernel": {"achieved": round(dn_bytes / (dn_ms / max(dn_n, 1) * 1e-3) / 1e9, 1), "unit": "GB/s",
                         "ms_per_launch": round(dn_ms / max(dn_n, 1), 5)},
         "stage_ms": stages,
@@ -304,7 +348,8 @@ def run_sweep(args):
     W = G.gen_weights(wl, device="cuda")
     layer = LatentMoE(cfg, W, max_tokens=max(Ts))
     pk = peaks()
-    flops_per_token = 1_436_811_264
+    A = accounting(cfg)
+    flops_per_token = A["flops_per_token"]
     for T in Ts:
         wlT = replace(wl, T=T, name=f"k3_sweep_t{T}")
         xs = [G.gen_x(replace(wlT, seed=wl.seed + 7919 * (i + 1)), device="cuda") for i in range(4)]
@@ -333,10 +378,9 @@ def run_sweep(args):
         layer.lmoe_set_profiling(0)
         layer.lmoe_sync_status()
         U_mean = sum(U[i % 4] for i in range(steps)) / steps
-        layer_bytes = DENSE_BYTES + U_mean * EXPERT_BYTES + T * TOKEN_IO_BYTES
-        din, F, k = cfg.d_latent, cfg.d_expert_ff, cfg.top_k
-        gu_bytes = U_mean * 2 * (F * din // 2 + F * din // 32)
-        dn_bytes = U_mean * (din * F // 2 + din * F // 32)
+        layer_bytes = A["dense"] + U_mean * A["expert"] + T * A["token_io"]
+        gu_bytes = U_mean * A["gu_w"]
+        dn_bytes = U_mean * A["dn_w"]
         gu = prof["expert_gate_up"][0] / max(prof["expert_gate_up"][1], 1)
         dn = prof["expert_down"][0] / max(prof["expert_down"][1], 1)
         tflops = T * flops_per_token / (ms * 1e-3) / 1e12
@@ -353,81 +397,96 @@ def run_sweep(args):
 
 
 # ------------------------------------------------------------- reference
+class ReferenceArm:
+    """The fp64 oracle restated one (token, slot) assignment at a time, for
+    the reference arm.  step(s) handles assignment s = t*k + j: at slot 0 it
+    also runs token t's latent down-projection (latent layers) and shared
+    MLP, at the last slot its RMSNorm and up-projection (latent layers);
+    every step dequantises and applies one routed expert afresh.  The router
+    runs on all tokens up front and the needed expert codes are generated
+    before timing (input preparation).  delta[t] holds each finished token's
+    Delta; a CPU test checks it against oracle.forward."""
+
+    def __init__(self, wl, n_assign: int, dev: str = "cpu", x_seed_offset: int = 7919):
+        import numpy as np
+        import torch
+        from lmoe_inputs import generate as G
+        import oracle as O
+        self.O, self.np = O, np
+        self.cfg = cfg = wl.cfg
+        self.k = k = cfg.top_k
+        ntok = (n_assign + k - 1) // k + 1
+        x = G.gen_x(replace(wl, seed=wl.seed + x_seed_offset), device="cpu", T=ntok)
+        self.x_bits = x.view(torch.int16).numpy().view(np.uint16)
+        Wn = O.numpy_inputs({n: t.cpu() for n, t in G.gen_dense_weights(wl, device=dev).items()})
+        self.layer = layer = O.Layer(cfg, Wn)
+        for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w"):
+            if name in Wn:
+                layer.dense(name)
+        for name in ("sh_gate", "sh_up", "sh_down"):
+            if name in Wn:
+                layer.shared(name)
+        self.xo = O.bf16_bits_to_f64(self.x_bits)
+        self.routes = O.router(self.xo, layer.dense("router_w"), Wn["router_bias"], k, cfg.routed_scale)
+        self.need = {}
+        for s in range(n_assign):
+            t, j = divmod(s, k)
+            e = int(self.routes["idx"][t, j])
+            for m in ("ex_gate", "ex_up", "ex_down"):
+                if (m, e) not in self.need:
+                    q, sc = G.gen_expert(wl, m, e, device=dev)
+                    self.need[(m, e)] = (q.cpu().numpy(), sc.cpu().numpy())
+        self.dequant = O.dequant_mxfp4 if cfg.expert_wfmt == "mxfp4" else O.dequant_fp8_block128
+        self.state = {}
+        self.delta = {}
+
+    def step(self, s: int) -> None:
+        cfg, layer, st, O = self.cfg, self.layer, self.state, self.O
+        t, j = divmod(s, self.k)
+        if j == 0:
+            x = self.xo[t]
+            st["xe"] = x @ layer.dense("w_down_latent").T if cfg.d_latent else x
+            st["u"] = self.np.zeros(st["xe"].shape[0])
+            if cfg.d_shared_ff:
+                g = x @ layer.shared("sh_gate").T
+                u = x @ layer.shared("sh_up").T
+                st["ys"] = layer.act(g, u) @ layer.shared("sh_down").T
+            else:
+                st["ys"] = 0.0
+        e = int(self.routes["idx"][t, j])
+        Wg = self.dequant(*self.need[("ex_gate", e)])
+        Wu = self.dequant(*self.need[("ex_up", e)])
+        Wd = self.dequant(*self.need[("ex_down", e)])
+        h = layer.act(Wg @ st["xe"], Wu @ st["xe"])
+        st["u"] += self.routes["G"][t, j] * (Wd @ h)
+        if j == self.k - 1:
+            if cfg.d_latent:
+                uh = O.rms_norm(st["u"], layer.dense("norm_w"), cfg.norm_eps) if cfg.use_latent_norm else st["u"]
+                yr = uh @ layer.dense("w_up_latent").T
+            else:
+                yr = st["u"]
+            self.delta[t] = yr + st["ys"]
+
+
 def run_reference(args):
-    """The fp64 oracle as the reference arm, on the host cores.  One step is
-    one (token, slot) assignment: the step at slot 0 also runs the token's
-    router, latent down-projection and shared MLP, the step at the last slot
-    its RMSNorm and up-projection; every step dequantises and applies one
-    routed expert afresh.  k steps = one token."""
+    """The fp64 oracle as the reference arm, on the host cores (ReferenceArm):
+    one step = one (token, slot) assignment, k steps = one token."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
     import torch
     from lmoe_inputs import configs as C
-    from lmoe_inputs import generate as G
-    import oracle as O
 
     wl = C.workload(args.workload)
     cfg = wl.cfg
     k = cfg.top_k
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    ntok = (args.warmup + args.steps + k - 1) // k + 1
-    x = G.gen_x(replace(wl, seed=wl.seed + 7919), device="cpu", T=max(ntok, 1))
-    W_dense = {}
-    for name, shape, fan in (("router_w", (cfg.n_experts, cfg.d_model), cfg.d_model),
-                             ("w_down_latent", (cfg.d_latent, cfg.d_model), cfg.d_model),
-                             ("w_up_latent", (cfg.d_model, cfg.d_latent), cfg.d_latent),
-                             ("sh_gate", (cfg.d_shared_ff, cfg.d_model), cfg.d_model),
-                             ("sh_up", (cfg.d_shared_ff, cfg.d_model), cfg.d_model),
-                             ("sh_down", (cfg.d_model, cfg.d_shared_ff), cfg.d_shared_ff)):
-        W_dense[name] = G.gen_dense(wl, name, shape, fan, device=dev).cpu()
-    W_dense["router_bias"] = G.gen_router_bias(wl)
-    W_dense["norm_w"] = G.to_bf16(1.0 + G.normal_f32(cfg.d_latent, G.stream_key(wl.seed, G.TAG["norm_w"]), "cpu",
-                                                     0.02))
-    Wn = O.numpy_inputs(W_dense)
-    xb = x.view(torch.int16).numpy().view(np.uint16)
-    layer = O.Layer(cfg, Wn)
-    for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w", "sh_gate", "sh_up", "sh_down"):
-        layer.dense(name)
-    xo = O.bf16_bits_to_f64(xb)
-    routes = O.router(xo, layer.dense("router_w"), Wn["router_bias"], k, cfg.routed_scale)
-    # expert codes of every assignment the run touches (input preparation, untimed)
     total = args.warmup + args.steps
-    need = {}
-    for s in range(total):
-        t, j = divmod(s, k)
-        e = int(routes["idx"][t, j])
-        for m in ("ex_gate", "ex_up", "ex_down"):
-            if (m, e) not in need:
-                q, sc = G.gen_expert(wl, m, e, device=dev)
-                need[(m, e)] = (q.cpu().numpy(), sc.cpu().numpy())
-
-    state = {}
-
-    def step(s):
-        t, j = divmod(s, k)
-        if j == 0:
-            state["xc"] = xo[t] @ layer.dense("w_down_latent").T
-            state["u"] = np.zeros(cfg.d_latent)
-            g = xo[t] @ layer.dense("sh_gate").T
-            u = xo[t] @ layer.dense("sh_up").T
-            state["ys"] = layer.act(g, u) @ layer.dense("sh_down").T
-        e = int(routes["idx"][t, j])
-        Wg = O.dequant_mxfp4(*need[("ex_gate", e)])
-        Wu = O.dequant_mxfp4(*need[("ex_up", e)])
-        Wd = O.dequant_mxfp4(*need[("ex_down", e)])
-        h = layer.act(Wg @ state["xc"], Wu @ state["xc"])
-        state["u"] += routes["G"][t, j] * (Wd @ h)
-        if j == k - 1:
-            uh = O.rms_norm(state["u"], layer.dense("norm_w"), cfg.norm_eps)
-            state["delta"] = uh @ layer.dense("w_up_latent").T + state["ys"]
-
+    arm = ReferenceArm(wl, total, dev="cuda" if torch.cuda.is_available() else "cpu")
     for s in range(args.warmup):
-        step(s)
+        arm.step(s)
     t0 = time.perf_counter()
     for s in range(args.warmup, total):
-        step(s)
+        arm.step(s)
     dt = time.perf_counter() - t0
     value = (args.steps / k) / dt
     line = {

@@ -72,6 +72,9 @@ WORKLOADS = {
 # Kimi-K3 shapes with 64 experts (1.1 GB of expert weights): the small case
 # for detailed profiler captures of the same kernels.
 WORKLOADS["k3_e64_t8"] = Workload("k3_e64_t8", replace(K3, n_experts=64), T=8, seed=6)
+# Kimi-K2 shapes with 32 experts (1.4 GB of FP8 expert weights) and 96
+# assignments per expert, near the 85 of the K2 T = 4096 batch.
+WORKLOADS["k2_e32_t384"] = Workload("k2_e32_t384", replace(K2, n_experts=32), T=384, seed=8)
 SWEEP_T = (1, 8, 32, 128, 512, 2048)
 for _t in SWEEP_T:
     WORKLOADS[f"k3_sweep_t{_t}"] = Workload(f"k3_sweep_t{_t}", K3, T=_t, seed=4)

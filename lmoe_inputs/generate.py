@@ -233,10 +233,12 @@ def gen_shared_fp8(wl: Workload, name: str, device="cpu"):
     return quantise_fp8_block128(w)
 
 
-def gen_weights(wl: Workload, device="cpu") -> dict:
-    """All layer weights on `device`.  Keys mirror the C-ABI weight struct."""
+def gen_dense_weights(wl: Workload, device="cpu") -> dict:
+    """The layer's non-expert weights on `device`: router, latent
+    projections and norm, shared MLP (bf16, or FP8 block-128 for the FP8
+    layer format)."""
     cfg = wl.cfg
-    d, l, E, F, Fs = cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.d_expert_ff, cfg.d_shared_ff
+    d, l, E, Fs = cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.d_shared_ff
     W = {}
     W["router_w"] = gen_dense(wl, "router_w", (E, d), d, device)
     W["router_bias"] = gen_router_bias(wl).to(device)
@@ -246,6 +248,22 @@ def gen_weights(wl: Workload, device="cpu") -> dict:
         if cfg.use_latent_norm:
             nw = 1.0 + normal_f32(l, stream_key(wl.seed, TAG["norm_w"]), "cpu", 0.02)
             W["norm_w"] = to_bf16(nw).to(device)
+    if Fs:
+        if cfg.expert_wfmt == "mxfp4":
+            W["sh_gate"] = gen_dense(wl, "sh_gate", (Fs, d), d, device)
+            W["sh_up"] = gen_dense(wl, "sh_up", (Fs, d), d, device)
+            W["sh_down"] = gen_dense(wl, "sh_down", (d, Fs), Fs, device)
+        else:
+            for name in ("sh_gate", "sh_up", "sh_down"):
+                W[name], W[name + "_s"] = gen_shared_fp8(wl, name, device)
+    return W
+
+
+def gen_weights(wl: Workload, device="cpu") -> dict:
+    """All layer weights on `device`.  Keys mirror the C-ABI weight struct."""
+    cfg = wl.cfg
+    E = cfg.n_experts
+    W = gen_dense_weights(wl, device)
     for name in ("ex_gate", "ex_up", "ex_down"):
         if device != "cpu" and cfg.expert_wfmt == "mxfp4":
             W[name + "_q"], W[name + "_s"] = gen_experts_mxfp4(wl, name, device)
@@ -257,14 +275,6 @@ def gen_weights(wl: Workload, device="cpu") -> dict:
                 W[name + "_s"] = torch.empty((E,) + tuple(s.shape), dtype=s.dtype, device=device)
             W[name + "_q"][e] = q
             W[name + "_s"][e] = s
-    if Fs:
-        if cfg.expert_wfmt == "mxfp4":
-            W["sh_gate"] = gen_dense(wl, "sh_gate", (Fs, d), d, device)
-            W["sh_up"] = gen_dense(wl, "sh_up", (Fs, d), d, device)
-            W["sh_down"] = gen_dense(wl, "sh_down", (d, Fs), Fs, device)
-        else:
-            for name in ("sh_gate", "sh_up", "sh_down"):
-                W[name], W[name + "_s"] = gen_shared_fp8(wl, name, device)
     return W
 
 
