@@ -85,6 +85,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int dense_bn(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 int moe_bn(int T, int k, int E) { return moe_tile_tokens(static_cast<long long>(T) * k, E); }
+// Token tile of the routed expert GEMMs of this handle's weight format.
+int expert_bn(const lmoe_ctx* h, int T) {
+  return h->fp8 ? fp8_tile_tokens(static_cast<long long>(T) * h->k, h->E) : moe_bn(T, h->k, h->E);
+}
 
 // K splits of a dense GEMM: fill about one wave of CTAs, at least two
 // 64-wide k-blocks per split.
@@ -237,7 +241,8 @@ lmoe_status validate_cfg(const lmoe_config* c) {
   // MXFP4 experts: latent layers (Kimi K3); FP8 block-128 experts: non-latent layers (Kimi K2)
   if (c->expert_wfmt == LMOE_W_MXFP4 && c->d_latent == 0) return LMOE_ERR_UNSUPPORTED;
   if (c->expert_wfmt == LMOE_W_FP8_BLOCK128 &&
-      (c->d_latent != 0 || c->use_latent_norm || c->d_model % 128 || c->d_expert_ff % 128 || c->d_shared_ff % 128))
+      (c->d_latent != 0 || c->use_latent_norm || c->d_model % 128 || c->d_expert_ff % 128 || c->d_shared_ff % 128 ||
+       c->d_model > kFp8MaxK || c->d_expert_ff > kFp8MaxK))
     return LMOE_ERR_UNSUPPORTED;
   if (c->d_model % 32 || c->d_latent % 32 || c->d_expert_ff % 32 || c->d_shared_ff % 32) return LMOE_ERR_UNSUPPORTED;
   if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
@@ -328,7 +333,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->KG_dn = h->Fp / 128;
   h->Tm = cfg->max_tokens;
   h->Pm = h->Tm * h->k;
-  const int bn_max = moe_bn(h->Tm, h->k, h->E);
+  const int bn_max = expert_bn(h, h->Tm);
   h->Ppad = h->Pm + h->E * (bn_max - 1);
   h->max_tiles = h->Pm / 16 + h->E + 1;
   h->nchunks_max = ceil_div(h->Pm, kDispatchChunk);
@@ -499,7 +504,7 @@ lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t
   if (T == 0) return LMOE_OK;
   if (!topk_idx || !counts || !offsets || !perm) return LMOE_ERR_INVALID_ARG;
   int launches = 0;
-  return run_dispatch(h, topk_idx, T, moe_bn(T, h->k, h->E), counts, offsets, perm, st, launches);
+  return run_dispatch(h, topk_idx, T, expert_bn(h, T), counts, offsets, perm, st, launches);
 }
 
 lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t* topk_idx_opt, float* topk_w_opt,
@@ -517,7 +522,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   lmoe_status s = run_router(h, x, T, st, launches);
   if (s != LMOE_OK) return s;
   // 3 dispatch
-  const int BNm = h->fp8 ? std::min(moe_bn(T, h->k, h->E), 32) : moe_bn(T, h->k, h->E);
+  const int BNm = expert_bn(h, T);
   s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
   if (s != LMOE_OK) return s;
 
@@ -550,9 +555,9 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
     if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->fp8, h->xq, h->xsf, st));
     else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, h->fp8, h->xq, h->xsf, st));
     ++launches;
     tm.done();
   }
@@ -560,7 +565,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
-    const int RB = h->fp8 ? fp8_rows_per_item(BNm) : moe_rows_per_item(BNm);
+    const int RB = h->fp8 ? kFp8Rows : moe_rows_per_item(BNm);
     const int mi = RB == 256 ? 1 : 0;
     p.a_gate = h->m_exg[mi];
     p.a_up = h->m_exu[mi];

@@ -67,21 +67,37 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
                             cudaStream_t s);
 
 // ------------------------------------------------------- routed experts
-// Activation rows of one assignment: two E4M3 rows (hi, lo) at padded row r
-// (rows 2r, 2r+1 of a [2*Ppad][Kp] byte matrix) and their scales in the
-// tcgen05 staging image, per BN-row tile and 128-wide k-group.
+// Activation rows of one assignment as two E4M3 rows (hi, lo) of a
+// [2*Ppad][Kp] byte matrix, with their E8M0 scales in the tcgen05 staging
+// image (512-byte atoms, one per 128 columns and 128-wide k-group).
+//   interleaved (split = 0): padded row r -> rows 2r (hi), 2r+1 (lo); the
+//     tile's 2*BN rows are one MMA operand of N = 2*BN columns, scale atoms
+//     [Ppad/BN][KG][ceil(2BN/128)].
+//   split (split = 1): per BN-row tile b, rows 2*BN*b + j (hi) and
+//     2*BN*b + BN + j (lo), j = r - BN*b; hi and lo are two operands of
+//     N = BN columns, scale atoms [Ppad/BN][KG][2] (BN <= 128).
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                                int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 // Same from bf16 token rows (layers whose experts take x itself).
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                                     int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 
 // Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
 // 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
 // prefill keep 128-row items so two accumulators fit tensor memory.
 __host__ __device__ constexpr int moe_rows_per_item(int BN) { return BN >= 64 ? 128 : 256; }
-// Weight rows per TMA box of the FP8-weight expert GEMMs.
-__host__ __device__ constexpr int fp8_rows_per_item(int BN) { return BN <= 16 ? 256 : 128; }
+// Weight rows per TMA box of the FP8-weight expert GEMMs (one fp32 scale block).
+constexpr int kFp8Rows = 128;
+// Largest contraction length of the FP8-weight expert GEMMs: the epilogue
+// holds an item's per-128-K block scales in two registers per lane.
+constexpr int kFp8MaxK = 64 * 128;
+// Token tile of the FP8-weight expert GEMMs (hi and lo share accumulator
+// columns, so a tile of up to 96 assignments fits tensor memory): the
+// smallest of 16, 32, 64, 96 that holds the mean assignments per expert.
+inline int fp8_tile_tokens(long long assignments, int n_experts) {
+  const long long m = (assignments + n_experts - 1) / n_experts;
+  return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 96;
+}
 // Token tile of the grouped expert GEMMs from the mean assignments per expert.
 inline int moe_tile_tokens(long long assignments, int n_experts) {
   return assignments <= 4LL * n_experts ? 16 : assignments <= 16LL * n_experts ? 32 : 64;

@@ -21,6 +21,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // CTAs at about the same time and read those weights through L2 once.  The
 // tiles of expert e are [tile_off[e]/BN, tile_off[e+1]/BN) and its items
 // [first*MT, (first+count)*MT), so tiles[w / MT] is one of expert e's tiles.
+// Split activation layout (see launch_quant_gather): the hi row of padded
+// assignment row r; its lo row is BN rows further.
+__host__ __device__ __forceinline__ size_t split_row_hi(int r, int BN) {
+  return static_cast<size_t>(r / BN) * 2 * BN + r % BN;
+}
+
 template <int BN>
 __device__ __forceinline__ int4 decode_item(const MoeGemmParams& p, int w, int& mt) {
   const int e = p.tiles[w / p.MT].x;

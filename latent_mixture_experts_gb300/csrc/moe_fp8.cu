@@ -1,55 +1,87 @@
 // Routed experts with FP8 E4M3 weights and fp32 scales per 128 x 128 block
 // (Kimi K2 card: the K2 checkpoint format; SwiGLU experts on the full width).
 //
-// Same pipeline as the MXFP4 kernel (TMA producer warp, single-thread MMA
-// issuer, four epilogue warps, persistent walk of the device tile list), on
-// block-scaled tcgen05 MMA (kind::mxf8f6f4, both operands E4M3).  The weight
-// scale is an fp32 number per 128 rows x 128 K, which an E8M0 scale cannot
-// carry, so the weights enter the MMA with unit scales and every 128-K group
-// is accumulated on its own: the MMA writes the group's partial product into
-// one of two TMEM buffers, and the epilogue warps add it, times that block's
-// fp32 scale, into register accumulators.  After the last group the item's
-// epilogue runs from those registers: SwiGLU (or SiTU) and the hi/lo E4M3
-// encoding of h for the gate/up pass, the routing weight for the down pass.
+// Persistent grouped GEMM over the device tile list: a TMA producer warp, a
+// single-thread tcgen05 MMA issuer (kind::mxf8f6f4, both operands E4M3) and
+// eight epilogue warps.  A work item is one 128-row block of gate and of up
+// weights (gate/up pass) or two 128-row blocks of down weights (down pass),
+// times one tile of up to 96 assignments.
+//
+// Activations are two E4M3 terms (hi + lo, each with an E8M0 scale per 32)
+// stored in the split layout: the tile's hi rows, then its lo rows.  Every
+// k-block issues one MMA on the hi rows and one on the lo rows into the SAME
+// accumulator columns, so tensor memory holds one column per assignment and
+// a 96-assignment tile fits; an expert's weights then pass through the SM
+// about once per expert instead of once per 32 assignments.
+//
+// The weight scale is an fp32 number per 128 rows x 128 K, which an E8M0
+// scale cannot carry, so the weights enter the MMA with unit scales and each
+// 128-K group is accumulated on its own into one buffer of a ring in tensor
+// memory; the epilogue warps add it, times that block's scale, into register
+// accumulators (two warps per 32-lane quarter, each owning half of the
+// tile's columns).  A work item's 128 rows share one scale per 128-K group,
+// so each lane holds the item's scales for groups lane and lane + 32 in
+// registers (fetched one item ahead) and a group's scale is a warp shuffle.
+// After the last group the item's epilogue runs from the registers: SwiGLU
+// (or SiTU) and the split hi/lo E4M3 encoding of h for the gate/up pass, the
+// routing weight for the down pass.
 #include "moe_common.cuh"
 
 namespace lmoe {
 
 namespace {
 
+constexpr int kFp8EpiWarps = 8;
+constexpr int kFp8Threads = 64 + 32 * kFp8EpiWarps;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+
 template <int BN, bool GU>
 struct Fp8Cfg {
-  static constexpr int N = 2 * BN;                   // hi/lo columns of BN assignments
-  static constexpr int RB = fp8_rows_per_item(BN);   // weight rows per TMA box
-  static constexpr int kTiles = RB / 128;
+  static constexpr int RB = kFp8Rows;                // weight rows per TMA box (one fp32 scale block)
   static constexpr int kBoxes = 2;                   // gate + up, or two down boxes
   static constexpr int IR = GU ? RB : 2 * RB;        // weight rows of one work item
-  static constexpr int kNAcc = kBoxes * kTiles;
+  static constexpr int kNAcc = kBoxes;
   static constexpr int kA = RB * 128;                // RB rows x 128 E4M3 codes
-  static constexpr int kB = N * 128;
+  static constexpr int kB = 2 * BN * 128;            // hi rows then lo rows
   static constexpr int kTile = kBoxes * kA + kB;
-  static constexpr int kSfb = 512;
+  static constexpr int kSfb = 1024;                  // hi and lo activation scale atoms
   static constexpr int kTx = kBoxes * kA + kB + kSfb;
-  static constexpr int kStages = RB == 256 ? 3 : 5;
+  static constexpr int kStagesFit = (227 * 1024 - 2048) / (kTile + kSfb);
+  static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
   static constexpr int kSmem = kStages * (kTile + kSfb) + 1024;
-  static constexpr int kPart = kNAcc * N;            // columns of one partial-product buffer
-  static constexpr int kSfaCol = 2 * kPart;          // constant unit weight scales (4 columns)
-  static constexpr int kSfbCol = kSfaCol + 4;        // activation scales, one slot per stage
-  static constexpr int kTmemUsed = kSfbCol + 4 * kStages;
+  static constexpr int kPart = kNAcc * BN;           // columns of one partial-product buffer
+  static constexpr int kRing = kPart <= 128 ? 3 : 2; // partial-product buffers
+  static constexpr int kSfaCol = kRing * kPart;      // constant unit weight scales (4 columns)
+  static constexpr int kSfbCol = kSfaCol + 4;        // activation scales, 8 columns per stage
+  static constexpr int kTmemUsed = kSfbCol + 8 * kStages;
   static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
-  static_assert(N <= 128, "one activation scale atom per stage");
+  static constexpr int kHalf = BN / 2;               // columns per epilogue warp
+  static constexpr int kLd = kHalf % 16 == 0 ? 16 : 8;
+  static_assert(BN % 16 == 0 && BN <= 128, "MMA N and one scale atom per half");
   static_assert(kTile % 1024 == 0, "tiles keep 1024-byte alignment");
+  static_assert(kStages >= 2, "pipeline depth");
   static_assert(kTmemUsed <= 512, "tensor memory budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  } else {
+    tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(v));
+  }
+}
+
+// 320 threads, one CTA per SM.  Registers are allocated per SM
+// sub-partition and one of the four holds three of the ten warps, so a
+// thread gets at most 168.
 template <int BN, bool GU>
-__global__ void __launch_bounds__(kThreads, 1) moe_fp8_kernel(const __grid_constant__ MoeGemmParams p) {
+__global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_constant__ MoeGemmParams p) {
   using C = Fp8Cfg<BN, GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* sf_region = sm + C::kStages * C::kTile;
-  __shared__ uint64_t full[C::kStages], empty[C::kStages], part_full[2], part_empty[2];
+  __shared__ uint64_t full[C::kStages], empty[C::kStages], part_full[C::kRing], part_empty[C::kRing];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -58,9 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_fp8_kernel(const __grid_const
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&part_full[i], 1);
-      mbar_init(&part_empty[i], kEpiWarps * 32);
+      mbar_init(&part_empty[i], kFp8EpiWarps * 32);
     }
     fence_mbar_init();
   }
@@ -72,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_fp8_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     // unit E8M0 scale (127) in every byte of the weight-scale columns
     const uint32_t one = 0x7F7F7F7Fu;
     tmem_st4(tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + C::kSfaCol, one, one, one, one);
@@ -130,23 +162,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_fp8_kernel(const __grid_const
             ok = false;
             break;
           }
-          const uint32_t pb = it & 1, use = it >> 1;
+          const uint32_t pb = it % C::kRing, use = it / C::kRing;
           if (use > 0 && !mbar_wait(&part_empty[pb], (use - 1) & 1, p.err, kErrTimeout)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfb = tbase + C::kSfbCol + 4 * s;
-          tmem_cp_32x128b_x4(sfb, sdesc_noswz(smem_u32(st_sfb(s)), 16, 128));
-          const uint32_t bb = smem_u32(st_b(s));
+          const uint32_t sfb_hi = tbase + C::kSfbCol + 8 * s, sfb_lo = sfb_hi + 4;
+          tmem_cp_32x128b_x4(sfb_hi, sdesc_noswz(smem_u32(st_sfb(s)), 16, 128));
+          tmem_cp_32x128b_x4(sfb_lo, sdesc_noswz(smem_u32(st_sfb(s) + 512), 16, 128));
+          const uint32_t b_hi = smem_u32(st_b(s)), b_lo = b_hi + BN * 128;
           const uint32_t d0 = tbase + pb * C::kPart;
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
-            const uint32_t idesc = idesc_mxf8f6f4(128, C::N, 0, 0, kb, kb);
+            const uint32_t idesc = idesc_mxf8f6f4(128, BN, 0, 0, kb, kb);
 #pragma unroll
             for (int i = 0; i < C::kNAcc; ++i) {
-              const uint32_t a_addr = smem_u32(st_a(s, i / C::kTiles)) + (i % C::kTiles) * 16384 + 32 * kb;
-              mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + 32 * kb), idesc, sfa, sfb, kb != 0);
+              const uint64_t a = sdesc_sw128(smem_u32(st_a(s, i)) + 32 * kb);
+              mma_mxf8f6f4(d0 + i * BN, a, sdesc_sw128(b_hi + 32 * kb), idesc, sfa, sfb_hi, kb != 0);
+              mma_mxf8f6f4(d0 + i * BN, a, sdesc_sw128(b_lo + 32 * kb), idesc, sfa, sfb_lo, true);
             }
           }
           mma_commit(&empty[s]);
@@ -155,97 +189,118 @@ __global__ void __launch_bounds__(kThreads, 1) moe_fp8_kernel(const __grid_const
       }
     }
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3;                       // 32-lane quarter of tensor memory
+    const int half = (warp - 2) >> 2;             // which half of the tile's columns
+    const int c_base = half * C::kHalf;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    // fp32 block scales of item w: accumulator i covers weight rows
+    // mt*IR + (down: i*RB), one 128-row block; lane l takes K groups l, l + 32.
+    auto item_scales = [&](int w, float (&out)[C::kNAcc][2]) {
+      int mt;
+      const int e = decode_item<BN>(p, w, mt).x;
+#pragma unroll
+      for (int i = 0; i < C::kNAcc; ++i) {
+        int rt = (mt * C::IR + (GU ? 0 : i * C::RB)) / 128;
+        rt = rt < p.NB ? rt : p.NB - 1;
+        const float* row = ((GU && i == 1) ? p.wsc1 : p.wsc0) + (static_cast<size_t>(e) * p.NB + rt) * p.KB;
+        out[i][0] = lane < KG ? __ldg(row + lane) : 0.f;
+        out[i][1] = lane + 32 < KG ? __ldg(row + lane + 32) : 0.f;
+      }
+    };
+    float scl[C::kNAcc][2] = {}, nscl[C::kNAcc][2] = {};
+    if (blockIdx.x < total) item_scales(blockIdx.x, scl);
     uint32_t it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       int mt;
       const int4 tile = decode_item<BN>(p, w, mt);
-      const int e = tile.x, row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      // fp32 block scale rows of the accumulators: box j, tile t -> rows mt*IR + j*RB(down)/0(gate,up) + 128t
-      const float* bsc[C::kNAcc];
-#pragma unroll
-      for (int i = 0; i < C::kNAcc; ++i) {
-        const int j = i / C::kTiles, t = i % C::kTiles;
-        int rt = (mt * C::IR + (GU ? 0 : j * C::RB) + t * 128) / 128;
-        rt = rt < p.NB ? rt : p.NB - 1;
-        bsc[i] = ((GU && j == 1) ? p.wsc1 : p.wsc0) + (static_cast<size_t>(e) * p.NB + rt) * p.KB;
-      }
-      float acc[C::kNAcc][C::N];
+      const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
+      if (w + static_cast<int>(gridDim.x) < total) item_scales(w + gridDim.x, nscl);
+      float acc[C::kNAcc][C::kHalf];
 #pragma unroll
       for (int i = 0; i < C::kNAcc; ++i)
 #pragma unroll
-        for (int c = 0; c < C::N; ++c) acc[i][c] = 0.f;
+        for (int c = 0; c < C::kHalf; ++c) acc[i][c] = 0.f;
       for (int g = 0; g < KG; ++g, ++it) {
-        float sc[C::kNAcc];
-#pragma unroll
-        for (int i = 0; i < C::kNAcc; ++i) sc[i] = __ldg(bsc[i] + g);
-        const uint32_t pb = it & 1;
-        if (!mbar_wait(&part_full[pb], (it >> 1) & 1, p.err, kErrTimeout)) {
+        const uint32_t pb = it % C::kRing;
+        if (!mbar_wait(&part_full[pb], (it / C::kRing) & 1, p.err, kErrTimeout)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < C::kNAcc; ++i) {
+          const float sc = __shfl_sync(0xFFFFFFFFu, g < 32 ? scl[i][0] : scl[i][1], g & 31);
+          const uint32_t col = tbase + lane_off + pb * C::kPart + i * BN + c_base;
+          // chunks of up to 32 columns: two loads in flight, one wait
 #pragma unroll
-          for (int c0 = 0; c0 < C::N; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tbase + lane_off + pb * C::kPart + i * C::N + c0, v);
+          for (int c0 = 0; c0 < C::kHalf; c0 += 32) {
+            constexpr int kW = 32;
+            uint32_t v[kW];
+            const int n = C::kHalf - c0 < kW ? C::kHalf - c0 : kW;
+#pragma unroll
+            for (int c = 0; c < kW; c += C::kLd)
+              if (c < n) tmem_ld_cols<C::kLd>(col + c0 + c, v + c);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 16; ++c) acc[i][c0 + c] = fmaf(sc[i], __uint_as_float(v[c]), acc[i][c0 + c]);
+            for (int c = 0; c < kW; ++c)
+              if (c < n) acc[i][c0 + c] = fmaf(sc, __uint_as_float(v[c]), acc[i][c0 + c]);
           }
         }
         tc_fence_before();
         mbar_arrive(&part_empty[pb]);
       }
+#pragma unroll
+      for (int i = 0; i < C::kNAcc; ++i) {
+        scl[i][0] = nscl[i][0];
+        scl[i][1] = nscl[i][1];
+      }
       if (!ok) break;
       if constexpr (GU) {
+        const int f = mt * C::RB + 32 * q + lane;
+        const bool f_ok = f < p.N_out;
+        const int kblk = f >> 5;
+        const int gf = kblk >> 2, kbf = kblk & 3;
+        const size_t hi0 = static_cast<size_t>(2) * row0;            // split layout: the tile's first hi row
+        uint8_t* atom = p.hsf + (static_cast<size_t>(row0 / BN) * (p.Fp / 128) + gf) * 1024;
 #pragma unroll
-        for (int t = 0; t < C::kTiles; ++t) {
-          if (mt * C::RB + t * 128 >= p.Fp) break;
-          const int f = mt * C::RB + t * 128 + 32 * q + lane;
-          const bool f_ok = f < p.N_out;
-          const int kblk = f >> 5;
-          const int g = kblk >> 2, kb = kblk & 3;
-#pragma unroll
-          for (int j = 0; j < BN; ++j) {
-            if (j < nrows) {                                   // warp-uniform
-              const float gv = acc[t][2 * j] + acc[t][2 * j + 1];
-              const float uv = acc[C::kTiles + t][2 * j] + acc[C::kTiles + t][2 * j + 1];
-              const float h = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
-              const HiLo hl = quant_hilo_warp(h);
-              const size_t r = static_cast<size_t>(row0) + j;
-              p.hq[(2 * r) * p.Fp + f] = hl.q_hi;
-              p.hq[(2 * r + 1) * p.Fp + f] = hl.q_lo;
-              if (lane == 0) {
-                const int n = 2 * j;
-                uint8_t* atom = p.hsf + (static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * 512;
-                atom[sf_atom_offset(n, kb)] = static_cast<uint8_t>(hl.s_hi);
-                atom[sf_atom_offset(n + 1, kb)] = static_cast<uint8_t>(hl.s_lo);
-              }
+        for (int j = 0; j < C::kHalf; ++j) {
+          const int jj = c_base + j;
+          if (jj < nrows) {                                            // warp-uniform
+            const float h = f_ok ? glu_act_fast(acc[0][j], acc[1][j], p.act, p.b1, p.b2) : 0.0f;
+            const HiLo hl = quant_hilo_warp(h);
+            p.hq[(hi0 + jj) * p.Fp + f] = hl.q_hi;
+            p.hq[(hi0 + BN + jj) * p.Fp + f] = hl.q_lo;
+            if (lane == 0) {
+              atom[sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl.s_hi);
+              atom[512 + sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl.s_lo);
             }
           }
         }
       } else {
-        int a_lo = 0;
-        float g_lo = 0.f;
-        if (lane < nrows) {
-          a_lo = p.perm[p0 + lane];
-          g_lo = p.G[a_lo];
+        constexpr int kR = (C::kHalf + 31) / 32;
+        int a_l[kR];
+        float g_l[kR];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+          const int jj = c_base + 32 * r + lane;
+          a_l[r] = 0;
+          g_l[r] = 0.f;
+          if (32 * r + lane < C::kHalf && jj < nrows) {
+            a_l[r] = p.perm[p0 + jj];
+            g_l[r] = p.G[a_l[r]];
+          }
         }
 #pragma unroll
         for (int i = 0; i < C::kNAcc; ++i) {
-          const int f = mt * C::IR + i * 128 + 32 * q + lane;
+          const int f = mt * C::IR + i * C::RB + 32 * q + lane;
           const bool f_ok = f < p.N_out;
 #pragma unroll
-          for (int j = 0; j < BN; ++j) {
-            if (j < nrows) {
-              const int a = __shfl_sync(0xFFFFFFFFu, a_lo, j);
-              const float gw = __shfl_sync(0xFFFFFFFFu, g_lo, j);
-              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = (acc[i][2 * j] + acc[i][2 * j + 1]) * gw;
+          for (int j = 0; j < C::kHalf; ++j) {
+            if (c_base + j < nrows) {
+              const int a = __shfl_sync(0xFFFFFFFFu, a_l[j / 32], j % 32);
+              const float gw = __shfl_sync(0xFFFFFFFFu, g_l[j / 32], j % 32);
+              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = acc[i][j] * gw;
             }
           }
         }
@@ -263,7 +318,7 @@ cudaError_t launch_fp8(const MoeGemmParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(moe_fp8_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  moe_fp8_kernel<BN, GU><<<grid, kThreads, C::kSmem, s>>>(p);
+  moe_fp8_kernel<BN, GU><<<grid, kFp8Threads, C::kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -285,6 +340,8 @@ cudaError_t launch_moe_fp8_gate_up(const MoeGemmParams& p, int BN, int grid, cud
   switch (BN) {
     case 16: return launch_fp8<16, true>(p, grid, s);
     case 32: return launch_fp8<32, true>(p, grid, s);
+    case 64: return launch_fp8<64, true>(p, grid, s);
+    case 96: return launch_fp8<96, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -292,6 +349,8 @@ cudaError_t launch_moe_fp8_down(const MoeGemmParams& p, int BN, int grid, cudaSt
   switch (BN) {
     case 16: return launch_fp8<16, false>(p, grid, s);
     case 32: return launch_fp8<32, false>(p, grid, s);
+    case 64: return launch_fp8<64, false>(p, grid, s);
+    case 96: return launch_fp8<96, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -281,8 +281,8 @@ cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
 // row's tile.
 template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
-                                    const int32_t* __restrict__ inv_pad, int BN, uint8_t* __restrict__ xq,
-                                    uint8_t* __restrict__ xsf) {
+                                    const int32_t* __restrict__ inv_pad, int BN, int split,
+                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nblk = Kp / 32;
   if (gw >= T * nblk) return;
@@ -293,6 +293,21 @@ __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, in
   const int NA = (2 * BN + 127) / 128;
   const int KG = Kp / 128;
   const int g = blk >> 2, kb = blk & 3;
+  if (split) {
+    for (int j = 0; j < k; ++j) {
+      const int r = inv_pad[static_cast<size_t>(t) * k + j];
+      const size_t row = split_row_hi(r, BN);
+      xq[row * Kp + c] = e.q_hi;
+      xq[(row + BN) * Kp + c] = e.q_lo;
+    }
+    for (int j = lane; j < k; j += 32) {
+      const int r = inv_pad[static_cast<size_t>(t) * k + j];
+      uint8_t* at = xsf + (static_cast<size_t>(r / BN) * KG + g) * 1024 + sf_atom_offset(r % BN, kb);
+      at[0] = static_cast<uint8_t>(e.s_hi);
+      at[512] = static_cast<uint8_t>(e.s_lo);
+    }
+    return;
+  }
   for (int j = 0; j < k; ++j) {
     const size_t r = static_cast<size_t>(inv_pad[static_cast<size_t>(t) * k + j]);
     xq[(2 * r) * Kp + c] = e.q_hi;
@@ -417,23 +432,23 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 }
 
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                                int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 32);
   quant_gather_kernel<float><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
-                               32 * warps_per_block, 0, s>>>(xc, T, k, din, Kp, inv_pad, BN, xq, xsf);
+                               32 * warps_per_block, 0, s>>>(xc, T, k, din, Kp, inv_pad, BN, split, xq, xsf);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                                     int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 32);
   quant_gather_kernel<__nv_bfloat16><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
                                        32 * warps_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, k, din,
-                                                                    Kp, inv_pad, BN, xq, xsf);
+                                                                    Kp, inv_pad, BN, split, xq, xsf);
   return cudaGetLastError();
 }
 
