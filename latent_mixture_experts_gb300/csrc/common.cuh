@@ -91,6 +91,36 @@ __device__ __forceinline__ HiLo quant_hilo_warp(float a) {
   return r;
 }
 
+// quant_hilo_warp on N independent values per lane (N tokens of the same
+// 32-block): the N warp reductions run interleaved, so their shuffle
+// latencies overlap.  Same result as N calls of quant_hilo_warp.
+template <int N>
+__device__ __forceinline__ void quant_hilo_warp_n(const float (&a)[N], HiLo (&r)[N]) {
+  float m[N], res[N];
+#pragma unroll
+  for (int u = 0; u < N; ++u) m[u] = fabsf(a[u]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    r[u].s_hi = e4m3_block_scale(m[u]);
+    r[u].q_hi = f32_to_e4m3(a[u] * e8m0_to_f32(254u - r[u].s_hi));
+    res[u] = a[u] - e4m3_to_f32(r[u].q_hi) * e8m0_to_f32(r[u].s_hi);
+    m[u] = fabsf(res[u]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    r[u].s_lo = e4m3_block_scale(m[u]);
+    r[u].q_lo = f32_to_e4m3(res[u] * e8m0_to_f32(254u - r[u].s_lo));
+  }
+}
+
 // Byte offset of one scale inside the tensor-memory staging image of a
 // 128-row (or 128-column) operand block: 32 lines of 16 bytes, line r0 holds
 // for c = 0..3 the four k-block scales of row 32c + r0.  This is the image

@@ -263,17 +263,26 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
         const int gf = kblk >> 2, kbf = kblk & 3;
         const size_t hi0 = static_cast<size_t>(2) * row0;            // split layout: the tile's first hi row
         uint8_t* atom = p.hsf + (static_cast<size_t>(row0 / BN) * (p.Fp / 128) + gf) * 1024;
+        // four tokens at a time: their activations and warp reductions overlap
 #pragma unroll
-        for (int j = 0; j < C::kHalf; ++j) {
-          const int jj = c_base + j;
-          if (jj < nrows) {                                            // warp-uniform
-            const float h = f_ok ? glu_act_fast(acc[0][j], acc[1][j], p.act, p.b1, p.b2) : 0.0f;
-            const HiLo hl = quant_hilo_warp(h);
-            p.hq[(hi0 + jj) * p.Fp + f] = hl.q_hi;
-            p.hq[(hi0 + BN + jj) * p.Fp + f] = hl.q_lo;
-            if (lane == 0) {
-              atom[sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl.s_hi);
-              atom[512 + sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl.s_lo);
+        for (int j0 = 0; j0 < C::kHalf; j0 += 4) {
+          if (c_base + j0 >= nrows) break;                             // warp-uniform
+          float h[4];
+          HiLo hl[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            h[u] = f_ok ? glu_act_fast(acc[0][j0 + u], acc[1][j0 + u], p.act, p.b1, p.b2) : 0.0f;
+          quant_hilo_warp_n<4>(h, hl);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int jj = c_base + j0 + u;
+            if (jj < nrows) {
+              p.hq[(hi0 + jj) * p.Fp + f] = hl[u].q_hi;
+              p.hq[(hi0 + BN + jj) * p.Fp + f] = hl[u].q_lo;
+              if (lane == 0) {
+                atom[sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl[u].s_hi);
+                atom[512 + sf_atom_offset(jj, kbf)] = static_cast<uint8_t>(hl[u].s_lo);
+              }
             }
           }
         }

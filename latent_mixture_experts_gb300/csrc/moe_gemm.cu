@@ -223,22 +223,34 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             tmem_ld_wait();
             const int kblk = f >> 5;                         // 32-feature block = this warp
             const int g = kblk >> 2, kb = kblk & 3;
+            // four tokens at a time: their activations and warp reductions overlap
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int j = j0 + jj;
-              if (j >= nrows) continue;                      // warp-uniform
-              const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
-              const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
-              const float h = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
-              const HiLo e = quant_hilo_warp(h);
-              const size_t r = static_cast<size_t>(row0) + j;
-              p.hq[(2 * r) * p.Fp + f] = e.q_hi;
-              p.hq[(2 * r + 1) * p.Fp + f] = e.q_lo;
-              if (lane == 0) {
-                const int n = 2 * j;                         // MMA column of the hi term in the down pass
-                uint8_t* atom = p.hsf + ((static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * C::NA) * 512;
-                atom[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
-                atom[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
+            for (int jq = 0; jq < 16; jq += 4) {
+              if (j0 + jq >= nrows) break;                   // warp-uniform
+              float h[4];
+              HiLo e[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int jj = jq + u;
+                const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
+                const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
+                h[u] = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
+              }
+              quant_hilo_warp_n<4>(h, e);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = j0 + jq + u;
+                if (j >= nrows) break;
+                const size_t r = static_cast<size_t>(row0) + j;
+                p.hq[(2 * r) * p.Fp + f] = e[u].q_hi;
+                p.hq[(2 * r + 1) * p.Fp + f] = e[u].q_lo;
+                if (lane == 0) {
+                  const int n = 2 * j;                       // MMA column of the hi term in the down pass
+                  uint8_t* atom = p.hsf + ((static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * C::NA) * 512;
+                  atom[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e[u].s_hi);
+                  atom[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] =
+                      static_cast<uint8_t>(e[u].s_lo);
+                }
               }
             }
           } else {
@@ -275,50 +287,91 @@ cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
 }
 
 // ------------------------------------------------------ activation encode
-// One warp per (token, 32-element block) of x^c: the hi/lo E4M3 codes are
-// computed once and written to the padded rows 2r, 2r+1 of each of the
-// token's k assignments; their scales go into the staging image of each
-// row's tile.
+// One warp per (token, 128-column group) of the expert input: each lane
+// encodes four consecutive values, a 32-value block is eight lanes, and the
+// hi/lo E4M3 codes are computed once and stored as one 4-byte word per lane
+// (a 128-byte row segment per warp) into every one of the token's k
+// assignment rows; the block scales go into the staging image of each row's
+// tile (launch_quant_gather gives both layouts).
+__device__ __forceinline__ float max8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+  return fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+}
+// Four consecutive inputs (din is a multiple of 32, so a lane's four values
+// are all inside the row or all past its end).
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  v[0] = q.x;
+  v[1] = q.y;
+  v[2] = q.z;
+  v[3] = q.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(q.x << 16);
+  v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(q.y << 16);
+  v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+}
+
 template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, int split,
                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int nblk = Kp / 32;
-  if (gw >= T * nblk) return;
-  const int t = gw / nblk, blk = gw % nblk;
-  const int c = blk * 32 + lane;
-  const float v = c < din ? static_cast<float>(xc[static_cast<size_t>(t) * din + c]) : 0.0f;
-  const HiLo e = quant_hilo_warp(v);
-  const int NA = (2 * BN + 127) / 128;
   const int KG = Kp / 128;
-  const int g = blk >> 2, kb = blk & 3;
+  if (gw >= T * KG) return;
+  const int t = gw / KG, g = gw % KG;
+  const int c0 = g * 128 + 4 * lane;
+  const int kb = lane >> 3;                                  // 32-value block of this lane
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (c0 < din) load4(xc + static_cast<size_t>(t) * din + c0, v);
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  const uint32_t s_hi = e4m3_block_scale(max8(m));
+  const float inv_hi = e8m0_to_f32(254u - s_hi), sc_hi = e8m0_to_f32(s_hi);
+  uint32_t w_hi = 0;
+  float res[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint8_t q = f32_to_e4m3(v[u] * inv_hi);
+    w_hi |= static_cast<uint32_t>(q) << (8 * u);
+    res[u] = v[u] - e4m3_to_f32(q) * sc_hi;
+  }
+  m = fmaxf(fmaxf(fabsf(res[0]), fabsf(res[1])), fmaxf(fabsf(res[2]), fabsf(res[3])));
+  const uint32_t s_lo = e4m3_block_scale(max8(m));
+  const float inv_lo = e8m0_to_f32(254u - s_lo);
+  uint32_t w_lo = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) w_lo |= static_cast<uint32_t>(f32_to_e4m3(res[u] * inv_lo)) << (8 * u);
+
+  const int32_t* rows = inv_pad + static_cast<size_t>(t) * k;
   if (split) {
     for (int j = 0; j < k; ++j) {
-      const int r = inv_pad[static_cast<size_t>(t) * k + j];
-      const size_t row = split_row_hi(r, BN);
-      xq[row * Kp + c] = e.q_hi;
-      xq[(row + BN) * Kp + c] = e.q_lo;
+      const size_t row = split_row_hi(rows[j], BN);
+      *reinterpret_cast<uint32_t*>(xq + row * Kp + c0) = w_hi;
+      *reinterpret_cast<uint32_t*>(xq + (row + BN) * Kp + c0) = w_lo;
     }
-    for (int j = lane; j < k; j += 32) {
-      const int r = inv_pad[static_cast<size_t>(t) * k + j];
+    for (int j = lane & 7; j < k; j += 8) {
+      const int r = rows[j];
       uint8_t* at = xsf + (static_cast<size_t>(r / BN) * KG + g) * 1024 + sf_atom_offset(r % BN, kb);
-      at[0] = static_cast<uint8_t>(e.s_hi);
-      at[512] = static_cast<uint8_t>(e.s_lo);
+      at[0] = static_cast<uint8_t>(s_hi);
+      at[512] = static_cast<uint8_t>(s_lo);
     }
     return;
   }
+  const int NA = (2 * BN + 127) / 128;
   for (int j = 0; j < k; ++j) {
-    const size_t r = static_cast<size_t>(inv_pad[static_cast<size_t>(t) * k + j]);
-    xq[(2 * r) * Kp + c] = e.q_hi;
-    xq[(2 * r + 1) * Kp + c] = e.q_lo;
+    const size_t r = static_cast<size_t>(rows[j]);
+    *reinterpret_cast<uint32_t*>(xq + (2 * r) * Kp + c0) = w_hi;
+    *reinterpret_cast<uint32_t*>(xq + (2 * r + 1) * Kp + c0) = w_lo;
   }
-  for (int j = lane; j < k; j += 32) {
-    const int r = inv_pad[static_cast<size_t>(t) * k + j];
+  for (int j = lane & 7; j < k; j += 8) {
+    const int r = rows[j];
     const int n = 2 * (r % BN);
     uint8_t* at = xsf + (static_cast<size_t>(r / BN) * KG + g) * NA * 512;
-    at[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e.s_hi);
-    at[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e.s_lo);
+    at[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(s_hi);
+    at[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(s_lo);
   }
 }
 
@@ -435,7 +488,7 @@ cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, 
                                 int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
-  const long long warps = static_cast<long long>(T) * (Kp / 32);
+  const long long warps = static_cast<long long>(T) * (Kp / 128);
   quant_gather_kernel<float><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
                                32 * warps_per_block, 0, s>>>(xc, T, k, din, Kp, inv_pad, BN, split, xq, xsf);
   return cudaGetLastError();
@@ -445,7 +498,7 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
                                      int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
-  const long long warps = static_cast<long long>(T) * (Kp / 32);
+  const long long warps = static_cast<long long>(T) * (Kp / 128);
   quant_gather_kernel<__nv_bfloat16><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
                                        32 * warps_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, k, din,
                                                                     Kp, inv_pad, BN, split, xq, xsf);
