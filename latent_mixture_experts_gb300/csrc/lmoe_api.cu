@@ -523,6 +523,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   if (s != LMOE_OK) return s;
   // 3 dispatch
   const int BNm = expert_bn(h, T);
+  const int split = h->fp8 || moe_split(BNm);   // activation layout the expert GEMMs read
   s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
   if (s != LMOE_OK) return s;
 
@@ -555,9 +556,9 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
     if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->fp8, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, st));
     else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, h->fp8, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, st));
     ++launches;
     tm.done();
   }

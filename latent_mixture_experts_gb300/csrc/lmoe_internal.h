@@ -98,10 +98,17 @@ inline int fp8_tile_tokens(long long assignments, int n_experts) {
   const long long m = (assignments + n_experts - 1) / n_experts;
   return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 96;
 }
-// Token tile of the grouped expert GEMMs from the mean assignments per expert.
+// Token tile of the grouped MXFP4 expert GEMMs from the mean assignments per
+// expert: 16 or 32 (decode; interleaved hi/lo columns, 256-row boxes), 64 or
+// 96 (prefill; split hi/lo operands, 128-row items).
 inline int moe_tile_tokens(long long assignments, int n_experts) {
-  return assignments <= 4LL * n_experts ? 16 : assignments <= 16LL * n_experts ? 32 : 64;
+  return assignments <= 4LL * n_experts ? 16 : assignments <= 16LL * n_experts ? 32
+         : assignments <= 64LL * n_experts ? 64 : 96;
 }
+// Activation layout of the grouped MXFP4 expert GEMMs at a token tile: split
+// (hi and lo as two MMAs into the same accumulator columns) for the large
+// tiles, interleaved (hi/lo as adjacent columns of one MMA) for the small.
+__host__ __device__ constexpr bool moe_split(int BN) { return BN >= 64; }
 
 struct MoeGemmParams {
   CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp] (boxes of moe_rows_per_item rows);

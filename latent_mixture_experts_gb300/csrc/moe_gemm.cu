@@ -30,21 +30,23 @@ namespace {
 
 template <int BN, bool GU>
 struct MoeCfg {
-  static constexpr int N = 2 * BN;                   // MMA N: hi/lo columns of BN assignments
-  static constexpr int NA = (N + 127) / 128;         // 128-column scale atoms of B
+  static constexpr bool SPLIT = moe_split(BN);       // hi and lo as two MMAs into one accumulator
+  static constexpr int N = SPLIT ? BN : 2 * BN;      // MMA N (columns per assignment: 1 split, 2 interleaved)
+  static constexpr int NA = SPLIT ? 2 : (N + 127) / 128;   // 512-byte scale atoms of B per stage
   static constexpr int RB = moe_rows_per_item(BN);   // weight rows per work item and TMA box
   static constexpr int kTiles = RB / 128;            // 128-row MMA tiles per box
   static constexpr int kBoxes = 2;                   // A boxes per stage: gate + up, or two down boxes
   static constexpr int IR = GU ? RB : 2 * RB;        // weight rows of one work item
   static constexpr int kNAcc = kBoxes * kTiles;      // accumulators per work item
   static constexpr int kA = RB * 128;                // one box: RB rows x 128 FP4 codes in 16-byte slots
-  static constexpr int kB = N * 128;                 // N rows x 128 E4M3 codes
+  static constexpr int kB = 2 * BN * 128;            // 2*BN rows (hi and lo) x 128 E4M3 codes
   static constexpr int kTile = kBoxes * kA + kB;     // swizzled tiles of one stage (multiple of 1024)
   static constexpr int kSfa = kTiles * 512;          // scale atoms of one box (adjacent in memory)
   static constexpr int kSfb = NA * 512;
   static constexpr int kSf = kBoxes * kSfa + kSfb;   // scale atoms of one stage
   static constexpr int kTx = kBoxes * (kA / 2) + kB + kSf;   // bytes the stage's copies deliver
-  static constexpr int kStages = RB == 256 ? 3 : 4;
+  static constexpr int kStagesFit = (227 * 1024 - 2048) / (kTile + kSf);
+  static constexpr int kStages = RB == 256 ? 3 : (kStagesFit < 4 ? kStagesFit : 4);
   static constexpr int kSmem = kStages * (kTile + kSf) + 1024;
   static constexpr int kAcc = kNAcc * N;             // accumulator columns of one buffer
   static constexpr int kSfCols = kNAcc * 4 + NA * 4; // scale columns per stage
@@ -168,6 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             for (int i = 0; i < C::kNAcc; ++i) {
               const uint32_t a_addr = smem_u32(st_a(s, i / C::kTiles)) + (i % C::kTiles) * 16384 + 32 * kb;
               mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + 32 * kb), idesc, sf + 4 * i, sfb, acc);
+              if constexpr (C::SPLIT)   // lo rows follow the tile's BN hi rows
+                mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + BN * 128 + 32 * kb), idesc,
+                             sf + 4 * i, sfb + 4, 1u);
             }
           }
           mma_commit(&empty[s]);
@@ -187,17 +192,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       int mt;
       const int4 tile = decode_item<BN>(p, w, mt);
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      // down pass: assignment and routing weight of the tile's rows j = lane, lane + 32
-      int a_lo = 0, a_hi = 0;
-      float g_lo = 0.f, g_hi = 0.f;
-      if (!GU) {
-        if (lane < nrows) {
-          a_lo = p.perm[p0 + lane];
-          g_lo = p.G[a_lo];
-        }
-        if (BN > 32 && lane + 32 < nrows) {
-          a_hi = p.perm[p0 + lane + 32];
-          g_hi = p.G[a_hi];
+      // down pass: assignment and routing weight of the tile's rows j = lane + 32r
+      constexpr int kR = (BN + 31) / 32;
+      int a_r[kR];
+      float g_r[kR];
+#pragma unroll
+      for (int r = 0; r < kR; ++r) {
+        a_r[r] = 0;
+        g_r[r] = 0.f;
+        if (!GU && lane + 32 * r < nrows) {
+          a_r[r] = p.perm[p0 + lane + 32 * r];
+          g_r[r] = p.G[a_r[r]];
         }
       }
       const uint32_t acc_base = tbase + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAcc;
@@ -208,6 +213,58 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (GU && mt * C::RB + t * 128 >= p.Fp) break;
         const int f = mt * C::IR + t * 128 + 32 * q + lane;   // output feature of this lane
         const bool f_ok = f < p.N_out;
+        if constexpr (C::SPLIT) {
+          // one column per assignment: gate (or down) at acc_base + t*N + j, up kTiles*N further
+#pragma unroll 1
+          for (int j0 = 0; j0 < BN; j0 += 16) {
+            if (j0 >= nrows) break;
+            uint32_t rg[16];
+            const uint32_t a0 = acc_base + t * C::N + j0;
+            tmem_ld16(a0, rg);
+            if constexpr (GU) {
+              uint32_t ru[16];
+              tmem_ld16(a0 + C::kTiles * C::N, ru);
+              tmem_ld_wait();
+              const int kblk = f >> 5;
+              const int g = kblk >> 2, kb = kblk & 3;
+              const size_t hi0 = static_cast<size_t>(2) * row0;      // the tile's first hi row
+              uint8_t* atom = p.hsf + (static_cast<size_t>(row0 / BN) * (p.Fp / 128) + g) * 1024;
+#pragma unroll
+              for (int jq = 0; jq < 16; jq += 4) {
+                if (j0 + jq >= nrows) break;                 // warp-uniform
+                float h[4];
+                HiLo e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  h[u] = f_ok ? glu_act_fast(__uint_as_float(rg[jq + u]), __uint_as_float(ru[jq + u]), p.act, p.b1,
+                                             p.b2)
+                              : 0.0f;
+                quant_hilo_warp_n<4>(h, e);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int j = j0 + jq + u;
+                  if (j >= nrows) break;
+                  p.hq[(hi0 + j) * p.Fp + f] = e[u].q_hi;
+                  p.hq[(hi0 + BN + j) * p.Fp + f] = e[u].q_lo;
+                  if (lane == 0) {
+                    atom[sf_atom_offset(j, kb)] = static_cast<uint8_t>(e[u].s_hi);
+                    atom[512 + sf_atom_offset(j, kb)] = static_cast<uint8_t>(e[u].s_lo);
+                  }
+                }
+              }
+            } else {
+              tmem_ld_wait();
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const int j = j0 + jj;
+                if (j >= nrows) break;
+                const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
+                const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
+                if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __uint_as_float(rg[jj]) * gw;
+              }
+            }
+          }
+        } else {
 #pragma unroll 1
         for (int j0 = 0; j0 < BN; j0 += 16) {
           if (j0 >= nrows) break;
@@ -259,12 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             for (int jj = 0; jj < 16; ++jj) {
               const int j = j0 + jj;
               if (j >= nrows) continue;
-              const int a = __shfl_sync(0xFFFFFFFFu, j < 32 ? a_lo : a_hi, j & 31);
-              const float gw = __shfl_sync(0xFFFFFFFFu, j < 32 ? g_lo : g_hi, j & 31);
+              const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
+              const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
               const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
               if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
             }
           }
+        }
         }
       }
       tc_fence_before();
@@ -472,6 +530,7 @@ cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStr
     case 16: return launch_moe<16, true>(p, grid, s);
     case 32: return launch_moe<32, true>(p, grid, s);
     case 64: return launch_moe<64, true>(p, grid, s);
+    case 96: return launch_moe<96, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -480,6 +539,7 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
     case 16: return launch_moe<16, false>(p, grid, s);
     case 32: return launch_moe<32, false>(p, grid, s);
     case 64: return launch_moe<64, false>(p, grid, s);
+    case 96: return launch_moe<96, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

