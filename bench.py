@@ -38,10 +38,24 @@ sys.path.insert(0, ROOT)
 
 METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
 UNIT = "tokens/s"
-# DRAM bytes per algorithmic byte of the K3 gate/up expert kernel, from one
-# ncu capture of the kernel as it stands (profiles/moe_gemm_k3_e64_t8.md).
-# None when the kernel has changed since the counters were taken.
-GU_DRAM_PER_ALGO_BYTE = None
+# DRAM bytes (read + write) per algorithmic byte of the gate/up expert
+# kernel of each weight format, from one ncu capture of the kernel as it
+# stands on a small case of the same instantiation (profiles/
+# moe_gemm_k3_e64_t8.md: 702.7 MB for 645.2 MB; profiles/
+# moe_fp8_k2_e32_t384.md: 1233.8 MB for 998.1 MB), keyed by (weight format,
+# token tile).  An entry is removed when its kernel changes until it is
+# captured again.
+GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.089, ("fp8_block128", 96): 1.236}
+
+
+def expert_tile(cfg, T: int) -> int:
+    """Token tile the library picks for the grouped expert GEMMs (the rule of
+    moe_tile_tokens / fp8_tile_tokens in the library's internal header)."""
+    P, E = T * cfg.top_k, cfg.n_experts
+    if cfg.expert_wfmt == "mxfp4":
+        return 16 if P <= 4 * E else 32 if P <= 16 * E else 64 if P <= 64 * E else 96
+    m = -(-P // E)
+    return 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 96
 
 
 def _mat_bytes(cfg, N: int, K: int) -> int:
@@ -261,7 +275,7 @@ def run_ours(args):
     dn_ms, dn_n = prof["expert_down"]
     layer_bytes = A["dense"] + U_mean * A["expert"] + T * A["token_io"]
     fp4 = cfg.expert_wfmt == "mxfp4"
-    gu_traffic = GU_DRAM_PER_ALGO_BYTE if fp4 else None
+    gu_traffic = GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
     stages = {name: round(v[0] / max(v[1], 1), 5) for name, v in prof.items()}
 
     # end to end through the host-buffer entry point
@@ -303,9 +317,10 @@ def run_ours(args):
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm"], 4),
                      "traffic": int(gu_traffic * gu_bytes) if gu_traffic else None,
-                     "traffic_source": "ncu dram__bytes_read+write of this kernel on the 64-expert K3-shaped case "
-                                       "(profiles/moe_gemm_k3_e64_t8.md), scaled to this launch by its algorithmic "
-                                       "bytes (active experts)",
+                     "traffic_source": ("ncu dram__bytes_read+write of this kernel on a small case of the same "
+                                        "instantiation (" + ("profiles/moe_gemm_k3_e64_t8.md" if fp4 else
+                                                             "profiles/moe_fp8_k2_e32_t384.md") +
+                                        "), scaled to this launch by its algorithmic bytes"),
                      "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_avg, 5),
                      "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"},
         "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),

@@ -39,3 +39,13 @@ def test_accounting_k2():
     assert a["expert"] == 3 * (2048 * 7168 + blk)
     assert a["dense"] == 384 * 7168 * 2 + 384 * 4 + 3 * (2048 * 7168 + blk)
     assert a["flops_per_token"] == 2 * 384 * 7168 + 8 * 6 * 2048 * 7168 + 6 * 2048 * 7168
+
+
+def test_expert_tile_rule():
+    """bench.py's copy of the library's token-tile rule picks the tiles the
+    profiler captures were taken on."""
+    assert bench.expert_tile(C.K3, 64) == 16
+    assert bench.expert_tile(C.workload("k3_e64_t8").cfg, 8) == 16
+    assert bench.expert_tile(C.K3, 8192) == 96
+    assert bench.expert_tile(C.K2, 4096) == 96
+    assert bench.expert_tile(C.workload("k2_e32_t384").cfg, 384) == 96
