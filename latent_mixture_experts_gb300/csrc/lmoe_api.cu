@@ -38,6 +38,7 @@ struct lmoe_ctx {
   size_t pool_bytes = 0;
   int* err = nullptr;
   float* part = nullptr;
+  float* part_sh = nullptr;   // split-K partials of the shared gate/up GEMM (runs on `side`)
   float* xc = nullptr;
   float* logits = nullptr;
   int32_t* idx = nullptr;
@@ -58,6 +59,11 @@ struct lmoe_ctx {
   // static tensor maps
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
   CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
+  // The shared-expert gate/up GEMM does not depend on the routing: it runs on
+  // a side stream forked from the caller's stream at the start of a forward
+  // and joined before the output GEMM that reads h_shared.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int last_T = 0;
   int last_launches = 0;
   // per-stage event timing
@@ -350,6 +356,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     const int nkb_o = ceil_div(h->din, 64) + (h->Fs ? ceil_div(h->Fs, 64) : 0);
     part_elems = std::max(part_elems, max_split_rows(ceil_div(h->d, 128), nkb_o, h->Tm, h->num_sms) * h->d);
   }
+  const long long part_sh_elems =
+      h->Fs ? max_split_rows(2 * ceil_div(h->Fs, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * 2LL * h->Fs : 0;
   const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
   const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
@@ -361,6 +369,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     Carve c;
     h->err = c.take<int>(4, base);
     h->part = c.take<float>(static_cast<size_t>(part_elems), base);
+    h->part_sh = c.take<float>(static_cast<size_t>(part_sh_elems), base);
     h->xc = c.take<float>(static_cast<size_t>(h->Tm) * h->din, base);
     h->logits = c.take<float>(static_cast<size_t>(h->Tm) * h->E, base);
     h->idx = c.take<int32_t>(h->Pm, base);
@@ -407,11 +416,18 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   carve(static_cast<char*>(h->pool));
 
   auto fail = [&](lmoe_status s) {
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     cudaFree(h->pool);
     delete h;
     return s;
   };
   if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  if (h->Fs && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess))
+    return fail(LMOE_ERR_CUDA);
   // expert weights: scale atoms, K padding when a reduction dim is not a multiple of 128
   const uint8_t* sg = static_cast<const uint8_t*>(w->ex_gate_s);
   const uint8_t* su = static_cast<const uint8_t*>(w->ex_up_s);
@@ -480,6 +496,9 @@ lmoe_status lmoe_destroy(lmoe_handle h) {
   cudaError_t e = cudaDeviceSynchronize();
   release_events(h);
   for (cudaEvent_t ev : h->ev_free) cudaEventDestroy(ev);
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
   cudaFree(h->pool);
   delete h;
   return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
@@ -518,6 +537,37 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   const int nt = ceil_div(T, BN);
   const int nkb_d = ceil_div(d, 64);
 
+  // 9 shared experts gate/up + SiTU, on the side stream: it needs only x, so
+  // it overlaps the router, dispatch and routed experts of the caller's stream
+  if (Fs) {
+    cudaStream_t ss = h->side;
+    LMOE_TRY(cudaEventRecord(h->ev_fork, st));
+    LMOE_TRY(cudaStreamWaitEvent(ss, h->ev_fork, 0));
+    StageTimer tm(h, LMOE_STAGE_SHARED, ss);
+    DenseParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a0 = h->m_shg;
+    p.a1 = h->m_shu;
+    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
+    p.mode = 1;
+    p.M0 = Fs;
+    p.M1 = Fs;
+    p.mtiles0 = ceil_div(Fs, 128);
+    p.T = T;
+    p.nkb = nkb_d;
+    p.nkb0 = nkb_d;
+    p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
+    p.ldo = 2 * Fs;
+    p.out = h->part_sh;
+    p.err = h->err;
+    LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, ss));
+    LMOE_TRY(launch_finalize_glu_bf16(h->part_sh, p.splits, T, Fs, 2 * Fs, h->h_s,
+                                      h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
+                                      h->cfg.situ_linear_beta, ss));
+    launches += 2;
+    tm.done();
+    LMOE_TRY(cudaEventRecord(h->ev_join, ss));
+  }
   // 1-2 router
   lmoe_status s = run_router(h, x, T, st, launches);
   if (s != LMOE_OK) return s;
@@ -626,32 +676,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     ++launches;
     tm.done();
   }
-  // 9 shared experts gate/up + SiTU
-  if (Fs) {
-    StageTimer tm(h, LMOE_STAGE_SHARED, st);
-    DenseParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.a0 = h->m_shg;
-    p.a1 = h->m_shu;
-    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
-    p.mode = 1;
-    p.M0 = Fs;
-    p.M1 = Fs;
-    p.mtiles0 = ceil_div(Fs, 128);
-    p.T = T;
-    p.nkb = nkb_d;
-    p.nkb0 = nkb_d;
-    p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
-    p.ldo = 2 * Fs;
-    p.out = h->part;
-    p.err = h->err;
-    LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, st));
-    LMOE_TRY(launch_finalize_glu_bf16(h->part, p.splits, T, Fs, 2 * Fs, h->h_s,
-                                      h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
-                                      h->cfg.situ_linear_beta, st));
-    launches += 2;
-    tm.done();
-  }
+  // join the shared gate/up GEMM of the side stream before the output GEMM reads h_shared
+  if (Fs) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_join, 0));
   // 10 Delta = u_hat W_up^T + h_shared W_shared_down^T
   if (din) {
     StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
