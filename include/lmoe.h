@@ -196,23 +196,28 @@ LMOE_API lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t stream);
 LMOE_API int lmoe_last_launch_count(lmoe_handle h);
 
 /* Per-stage timing.  While enabled, lmoe_forward records a CUDA event pair
- * on its stream around each stage below; lmoe_profile_get synchronises the
- * recorded events and returns the stage's summed device time (ms) and the
- * number of timed launches since profiling was last enabled.  Enabling
- * again resets the sums.  Stages: */
+ * on the stage's stream around each stage whose bit (1 << stage) is set in
+ * stage_mask (0 disables timing); lmoe_profile_get synchronises the recorded
+ * events and returns the stage's summed device time (ms) and the number of
+ * timed launches since profiling was last enabled.  Enabling again resets
+ * the sums.  reserve_forwards pre-creates event pairs for that many
+ * forwards.  An event between two kernels ends the overlap of the second
+ * kernel's start with the first one's drain, so timing every stage slows a
+ * small forward measurably; time only the stages of interest.  Stages: */
 enum {
   LMOE_STAGE_ROUTER = 0,     /* router GEMM + top-k */
   LMOE_STAGE_DISPATCH = 1,   /* counting-sort dispatch */
   LMOE_STAGE_LATENT_DOWN = 2,/* x^c GEMM (+ split-K sum) */
   LMOE_STAGE_ACT_QUANT = 3,  /* x^c -> hi/lo E4M3 in expert-tile order */
-  LMOE_STAGE_EXPERT_GU = 4,  /* grouped MXFP4 gate/up GEMM + SiTU */
-  LMOE_STAGE_EXPERT_DOWN = 5,/* grouped MXFP4 down GEMM x G */
+  LMOE_STAGE_EXPERT_GU = 4,  /* grouped expert gate/up GEMM (MXFP4 or FP8) + SiTU / SwiGLU */
+  LMOE_STAGE_EXPERT_DOWN = 5,/* grouped expert down GEMM x G */
   LMOE_STAGE_COMBINE = 6,    /* slot-ordered sum + RMSNorm */
-  LMOE_STAGE_SHARED = 7,     /* shared gate/up GEMM + SiTU */
+  LMOE_STAGE_SHARED = 7,     /* shared gate/up GEMM + SiTU (on the handle's side stream) */
   LMOE_STAGE_OUTPUT = 8,     /* [u_hat | h_shared] output GEMM */
   LMOE_NUM_STAGES = 9
 };
-LMOE_API lmoe_status lmoe_set_profiling(lmoe_handle h, int enable);
+#define LMOE_PROFILE_ALL_STAGES 0x1FFu
+LMOE_API lmoe_status lmoe_set_profiling(lmoe_handle h, int reserve_forwards, uint32_t stage_mask);
 LMOE_API lmoe_status lmoe_profile_get(lmoe_handle h, int stage, float* total_ms, int* count);
 
 /* Number of distinct experts the last lmoe_forward's batch selected

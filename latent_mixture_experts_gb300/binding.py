@@ -26,6 +26,7 @@ EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lm
            "lmoe_dispatch_noalloc")
 NOALLOC_MAX_ASSIGNMENTS = 65536
 NOALLOC_MAX_EXPERTS = 2048
+PROFILE_ALL_STAGES = 0x1FF
 STAGES = ("router", "dispatch", "latent_down", "act_quant", "expert_gate_up", "expert_down", "combine_norm",
           "shared", "output")
 
@@ -75,7 +76,7 @@ def load_library(path: str = LIB_PATH):
             "lmoe_debug_tensor": (I, [P, ctypes.c_char_p, P, S, P]),
             "lmoe_sync_status": (I, [P, P]),
             "lmoe_last_launch_count": (I, [P]),
-            "lmoe_set_profiling": (I, [P, I]),
+            "lmoe_set_profiling": (I, [P, I, ctypes.c_uint32]),
             "lmoe_profile_get": (I, [P, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
             "lmoe_last_active_experts": (I, [P, P]),
             "lmoe_destroy": (I, [P]),
@@ -214,8 +215,16 @@ class LatentMoE:
     def lmoe_last_launch_count(self) -> int:
         return int(self._lib.lmoe_last_launch_count(self._h))
 
-    def lmoe_set_profiling(self, reserve_forwards: int):
-        _check("lmoe_set_profiling", self._lib.lmoe_set_profiling(self._h, int(reserve_forwards)))
+    def lmoe_set_profiling(self, reserve_forwards: int, stages=None):
+        """Time the named stages (all when None) of the next forwards; an
+        empty list or reserve_forwards = 0 with stages=[] turns timing off."""
+        if stages is None:
+            mask = PROFILE_ALL_STAGES if reserve_forwards else 0
+        else:
+            mask = 0
+            for name in stages:
+                mask |= 1 << STAGES.index(name)
+        _check("lmoe_set_profiling", self._lib.lmoe_set_profiling(self._h, int(reserve_forwards), mask))
 
     def lmoe_profile_get(self) -> dict:
         """{stage name: (summed ms, launches)} since profiling was enabled."""

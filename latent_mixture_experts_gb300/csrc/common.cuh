@@ -121,6 +121,14 @@ __device__ __forceinline__ void quant_hilo_warp_n(const float (&a)[N], HiLo (&r)
   }
 }
 
+// Programmatic dependent launch: the kernels of a forward are launched with
+// programmatic stream serialization, so a kernel's CTAs may start while its
+// predecessor drains.  Each kernel lets its successor launch at once and,
+// before its first global read or write, waits until the predecessor grid
+// has completed and its memory is visible (a no-op without the attribute).
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Byte offset of one scale inside the tensor-memory staging image of a
 // 128-row (or 128-column) operand block: 32 lines of 16 bytes, line r0 holds
 // for c = 0..3 the four k-block scales of row 32c + r0.  This is the image

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
+  griddep_wait();
   const uint32_t tacc = tmem_base;
 
   if (warp == 0 && lane == 0) {
@@ -135,13 +137,18 @@ cudaError_t launch_bn(const DenseParams& p, int mtiles, cudaStream_t s) {
     attr_set = true;
   }
   dim3 grid(mtiles, (p.T + BN - 1) / BN, p.splits);
-  dense_gemm_kernel<BN><<<grid, 128, C::kSmem, s>>>(p);
+  {
+    const cudaError_t e_ = launch_pdl(dense_gemm_kernel<BN>, grid, 128, C::kSmem, s, p);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------- finalizers
 __global__ void finalize_sum_f32_kernel(const float* __restrict__ part, int splits, int T, int M, int ld,
                                         float* __restrict__ out, int ldo) {
+  griddep_launch();
+  griddep_wait();
   const size_t n = static_cast<size_t>(T) * M;
   const size_t plane = static_cast<size_t>(T) * ld;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
@@ -156,6 +163,8 @@ __global__ void finalize_sum_f32_kernel(const float* __restrict__ part, int spli
 __global__ void finalize_sum_bf16_kernel(const float* __restrict__ part, int splits, int T, int M, int ld,
                                          __nv_bfloat16* __restrict__ out, int ldo, const float* __restrict__ add,
                                          int ld_add) {
+  griddep_launch();
+  griddep_wait();
   const size_t n = static_cast<size_t>(T) * M;
   const size_t plane = static_cast<size_t>(T) * ld;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
@@ -170,6 +179,8 @@ __global__ void finalize_sum_bf16_kernel(const float* __restrict__ part, int spl
 
 __global__ void finalize_glu_bf16_kernel(const float* __restrict__ part, int splits, int T, int F, int ld,
                                          __nv_bfloat16* __restrict__ out, int act, float b1, float b2) {
+  griddep_launch();
+  griddep_wait();
   const size_t n = static_cast<size_t>(T) * F;
   const size_t plane = static_cast<size_t>(T) * ld;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
@@ -204,23 +215,33 @@ cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStre
 cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,
                                     cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * M;
-  finalize_sum_f32_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, M, ld, out, ldo);
+  {
+    const cudaError_t e_ = launch_pdl(finalize_sum_f32_kernel, ew_grid(n), 256, 0, s, part,
+                                      splits, T, M, ld, out, ldo);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M, int ld, void* out, int ldo,
                                      const float* add_opt, int ld_add, cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * M;
-  finalize_sum_bf16_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, M, ld,
-                                                     static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
+  {
+    const cudaError_t e_ = launch_pdl(finalize_sum_bf16_kernel, ew_grid(n), 256, 0, s, part,
+                                      splits, T, M, ld, static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_glu_bf16(const float* part, int splits, int T, int F, int ld, void* out, int act,
                                      float b1, float b2, cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * F;
-  finalize_glu_bf16_kernel<<<ew_grid(n), 256, 0, s>>>(part, splits, T, F, ld, static_cast<__nv_bfloat16*>(out),
-                                                     act, b1, b2);
+  {
+    const cudaError_t e_ = launch_pdl(finalize_glu_bf16_kernel, ew_grid(n), 256, 0, s, part,
+                                      splits, T, F, ld, static_cast<__nv_bfloat16*>(out), act, b1, b2);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

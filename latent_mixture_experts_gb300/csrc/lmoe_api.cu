@@ -68,6 +68,7 @@ struct lmoe_ctx {
   int last_launches = 0;
   // per-stage event timing
   bool prof = false;
+  uint32_t prof_mask = 0;    // stages timed while profiling
   std::vector<cudaEvent_t> ev_free;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_used[LMOE_NUM_STAGES];
 };
@@ -160,7 +161,7 @@ struct StageTimer {
   cudaStream_t st;
   cudaEvent_t b = nullptr;
   StageTimer(lmoe_ctx* h_, int stage_, cudaStream_t st_) : h(h_), stage(stage_), st(st_) {
-    if (h->prof && (b = take_event(h)) != nullptr) cudaEventRecord(b, st);
+    if (h->prof && (h->prof_mask >> stage & 1u) && (b = take_event(h)) != nullptr) cudaEventRecord(b, st);
   }
   void done() {
     if (!b) return;
@@ -799,12 +800,14 @@ lmoe_status lmoe_sync_status(lmoe_handle h, cudaStream_t st) {
 
 int lmoe_last_launch_count(lmoe_handle h) { return h ? h->last_launches : 0; }
 
-lmoe_status lmoe_set_profiling(lmoe_handle h, int enable) {
-  if (!h || enable < 0) return LMOE_ERR_INVALID_ARG;
+lmoe_status lmoe_set_profiling(lmoe_handle h, int reserve_forwards, uint32_t stage_mask) {
+  if (!h || reserve_forwards < 0) return LMOE_ERR_INVALID_ARG;
   release_events(h);
-  h->prof = enable > 0;
-  // enable > 0 also reserves event pairs for that many forwards
-  const size_t want = static_cast<size_t>(enable) * 2 * LMOE_NUM_STAGES;
+  h->prof_mask = stage_mask & LMOE_PROFILE_ALL_STAGES;
+  h->prof = h->prof_mask != 0;
+  int timed = 0;
+  for (int i = 0; i < LMOE_NUM_STAGES; ++i) timed += h->prof_mask >> i & 1u;
+  const size_t want = static_cast<size_t>(reserve_forwards) * 2 * timed;
   while (h->prof && h->ev_free.size() < want) {
     cudaEvent_t e = nullptr;
     LMOE_TRY(cudaEventCreate(&e));

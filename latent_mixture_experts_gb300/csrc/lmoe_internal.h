@@ -110,6 +110,24 @@ inline int moe_tile_tokens(long long assignments, int n_experts) {
 // tiles, interleaved (hi/lo as adjacent columns of one MMA) for the small.
 __host__ __device__ constexpr bool moe_split(int BN) { return BN >= 64; }
 
+// Launch `kernel` with programmatic stream serialization (see griddep_wait):
+// it may begin while the previous kernel on the stream drains.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct MoeGemmParams {
   CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp] (boxes of moe_rows_per_item rows);
                                  // activations [2*Ppad][Kp]

@@ -103,6 +103,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
+  griddep_wait();
   const uint32_t tbase = tmem_base;
   if (warp >= 2 && warp < 6) {
     // unit E8M0 scale (127) in every byte of the weight-scale columns
@@ -327,7 +329,10 @@ cudaError_t launch_fp8(const MoeGemmParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(moe_fp8_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  moe_fp8_kernel<BN, GU><<<grid, kFp8Threads, C::kSmem, s>>>(p);
+  {
+    const cudaError_t e_ = launch_pdl(moe_fp8_kernel<BN, GU>, grid, kFp8Threads, C::kSmem, s, p);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
+  griddep_wait();
   const uint32_t tbase = tmem_base;
 
   const int ntiles = *p.ntiles;
@@ -340,7 +342,10 @@ cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  moe_gemm_kernel<BN, GU><<<grid, kThreads, C::kSmem, s>>>(p);
+  {
+    const cudaError_t e_ = launch_pdl(moe_gemm_kernel<BN, GU>, grid, kThreads, C::kSmem, s, p);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -377,6 +382,8 @@ template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, int split,
                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
+  griddep_launch();
+  griddep_wait();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int KG = Kp / 128;
   if (gw >= T * KG) return;
@@ -441,6 +448,8 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restri
                                                            const __nv_bfloat16* __restrict__ w, int use_norm,
                                                            float eps, float* __restrict__ u_out,
                                                            __nv_bfloat16* __restrict__ u_hat) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ float4 cn_u4[];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -549,8 +558,12 @@ cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, 
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
-  quant_gather_kernel<float><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
-                               32 * warps_per_block, 0, s>>>(xc, T, k, din, Kp, inv_pad, BN, split, xq, xsf);
+  {
+    const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
+    const cudaError_t e_ = launch_pdl(quant_gather_kernel<float>, blocks, 32 * warps_per_block, 0, s, xc, T, k, din,
+                                      Kp, inv_pad, BN, split, xq, xsf);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -559,9 +572,13 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
-  quant_gather_kernel<__nv_bfloat16><<<static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block),
-                                       32 * warps_per_block, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, k, din,
-                                                                    Kp, inv_pad, BN, split, xq, xsf);
+  {
+    const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
+    const cudaError_t e_ = launch_pdl(quant_gather_kernel<__nv_bfloat16>, blocks, 32 * warps_per_block, 0, s,
+                                      static_cast<const __nv_bfloat16*>(x), T, k, din, Kp, inv_pad, BN, split, xq,
+                                      xsf);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -573,8 +590,12 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void*
     cudaError_t e = cudaFuncSetAttribute(combine_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  combine_norm_kernel<<<T, 512, smem, s>>>(y, T, k, l, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
-                                          static_cast<__nv_bfloat16*>(u_hat));
+  {
+    const cudaError_t e_ = launch_pdl(combine_norm_kernel, T, 512, smem, s, y,
+                                      T, k, l, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
+                                      static_cast<__nv_bfloat16*>(u_hat));
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

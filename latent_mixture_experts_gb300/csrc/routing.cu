@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
                                                             int E, const float* __restrict__ bias, int k,
                                                             float scale, int32_t* __restrict__ idx,
                                                             float* __restrict__ G, float* __restrict__ z_out) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ float tk_smem[];
   float* c = tk_smem;
   float* sg = tk_smem + E;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
                                                               int32_t* __restrict__ tile_off,
                                                               int4* __restrict__ tiles, int32_t* __restrict__ ntiles,
                                                               int* err) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t hist[kMaxExperts];
   __shared__ int32_t s_off[kMaxExperts + 1];
   __shared__ int32_t s_toff[kMaxExperts + 1];
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
 // Per-chunk histogram of expert ids.
 __global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int P, int E, int32_t* __restrict__ blockcnt,
                                       int* err) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -208,6 +214,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
                                                              int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ tile_off, int4* __restrict__ tiles,
                                                              int32_t* __restrict__ ntiles) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t s_cnt[kMaxExperts];
   __shared__ int32_t s_off[kMaxExperts + 1];
   __shared__ int32_t s_toff[kMaxExperts + 1];
@@ -261,6 +269,8 @@ __global__ void __launch_bounds__(32) dispatch_scatter_kernel(const int32_t* __r
                                                               const int32_t* __restrict__ tile_off,
                                                               int32_t* __restrict__ perm,
                                                               int32_t* __restrict__ inv_pad) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ int32_t pos[];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) pos[e] = blockcnt[static_cast<size_t>(blockIdx.x) * E + e];
@@ -291,7 +301,11 @@ cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const
                         float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const size_t smem = 2 * static_cast<size_t>(E) * sizeof(float);
-  topk_kernel<<<T, kTopkThreads, smem, s>>>(logit_part, splits, T, E, bias, k, routed_scale, idx, G, z_out);
+  {
+    const cudaError_t e_ = launch_pdl(topk_kernel, T, kTopkThreads, smem, s, logit_part,
+                                      splits, T, E, bias, k, routed_scale, idx, G, z_out);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
@@ -300,17 +314,31 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
   const int P = T * k;
   if (P <= 0) return cudaSuccess;
   if (P <= kSmallDispatch) {
-    dispatch_small_kernel<<<1, 1024, 0, s>>>(idx, P, E, BN, b.counts, b.offsets, b.perm, b.inv_pad, b.tile_off,
-                                             b.tiles, b.ntiles, b.err);
+    {
+      const cudaError_t e_ = launch_pdl(dispatch_small_kernel, 1, 1024, 0, s, idx,
+                                        P, E, BN, b.counts, b.offsets, b.perm, b.inv_pad, b.tile_off, b.tiles,
+                                        b.ntiles, b.err);
+      if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
   }
   const int nchunks = (P + kDispatchChunk - 1) / kDispatchChunk;
   const size_t hsmem = static_cast<size_t>(E) * sizeof(int32_t);
-  dispatch_count_kernel<<<nchunks, 256, hsmem, s>>>(idx, P, E, b.blockcnt, b.err);
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.blockcnt, nchunks, E, BN, b.counts, b.offsets, b.tile_off, b.tiles,
-                                          b.ntiles);
-  dispatch_scatter_kernel<<<nchunks, 32, hsmem, s>>>(idx, P, E, b.blockcnt, b.offsets, b.tile_off, b.perm,
-                                                     b.inv_pad);
+  {
+    const cudaError_t e_ = launch_pdl(dispatch_count_kernel, nchunks, 256, hsmem, s, idx,
+                                      P, E, b.blockcnt, b.err);
+    if (e_ != cudaSuccess) return e_;
+  }
+  {
+    const cudaError_t e_ = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, b.blockcnt,
+                                      nchunks, E, BN, b.counts, b.offsets, b.tile_off, b.tiles, b.ntiles);
+    if (e_ != cudaSuccess) return e_;
+  }
+  {
+    const cudaError_t e_ = launch_pdl(dispatch_scatter_kernel, nchunks, 32, hsmem, s, idx,
+                                      P, E, b.blockcnt, b.offsets, b.tile_off, b.perm, b.inv_pad);
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 
