@@ -60,9 +60,9 @@ struct DispatchBufs {
 };
 constexpr int kDispatchChunk = 256;
 // Batches of at most this many assignments are dispatched by one kernel;
-// larger ones by the three-kernel chunked path.
+// larger ones by the four-kernel chunked path.
 constexpr int kSmallDispatch = 8192;
-inline int dispatch_launches(int assignments) { return assignments <= kSmallDispatch ? 1 : 3; }
+inline int dispatch_launches(int assignments) { return assignments <= kSmallDispatch ? 1 : 4; }
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, const DispatchBufs& b,
                             cudaStream_t s);
 

@@ -207,58 +207,99 @@ __global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int P, in
   for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One block: per-expert prefix over chunks, exclusive scans over experts
-// (plain and BN-padded), the tile list.
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ blockcnt, int nchunks, int E,
-                                                             int BN, int32_t* __restrict__ counts,
+// One warp per expert: exclusive prefix of the expert's per-chunk counts, in
+// place, and the expert's total.  Lane l owns a contiguous run of chunks, so
+// the prefix is a warp scan of the 32 run sums plus a sequential pass.
+__global__ void __launch_bounds__(256) dispatch_chunkscan_kernel(int32_t* __restrict__ blockcnt, int nchunks, int E,
+                                                                 int32_t* __restrict__ counts) {
+  griddep_launch();
+  griddep_wait();
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;                                    // whole warp
+  const int per = (nchunks + 31) / 32;
+  const int b0 = min(nchunks, lane * per), b1 = min(nchunks, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += blockcnt[static_cast<size_t>(b) * E + e];
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  int run = incl - sum;
+  for (int b = b0; b < b1; ++b) {
+    const int c = blockcnt[static_cast<size_t>(b) * E + e];
+    blockcnt[static_cast<size_t>(b) * E + e] = run;
+    run += c;
+  }
+  if (lane == 31) counts[e] = incl;
+}
+
+// One block of 1024 threads, two experts per thread: exclusive scans over
+// the experts of the counts, the BN-padded counts and the tile counts
+// (offsets, tile_off, first tile), then the tile list.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __restrict__ counts, int E, int BN,
                                                              int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ tile_off, int4* __restrict__ tiles,
                                                              int32_t* __restrict__ ntiles) {
   griddep_launch();
   griddep_wait();
-  __shared__ int32_t s_cnt[kMaxExperts];
-  __shared__ int32_t s_off[kMaxExperts + 1];
-  __shared__ int32_t s_toff[kMaxExperts + 1];
-  __shared__ int32_t s_tiles[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nchunks; ++b) {
-      const int c = blockcnt[static_cast<size_t>(b) * E + e];
-      blockcnt[static_cast<size_t>(b) * E + e] = run;
-      run += c;
+  __shared__ int wsum[3][32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int e0 = 2 * t;
+  int c[2], n[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    c[j] = e0 + j < E ? counts[e0 + j] : 0;
+    n[j] = (c[j] + BN - 1) / BN;
+  }
+  const int own[3] = {c[0] + c[1], (n[0] + n[1]) * BN, n[0] + n[1]};
+  int inc[3] = {own[0], own[1], own[2]};
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, inc[q], off);
+      if (lane >= off) inc[q] += v;
     }
-    s_cnt[e] = run;
-    counts[e] = run;
+  if (lane == 31)
+#pragma unroll
+    for (int q = 0; q < 3; ++q) wsum[q][w] = inc[q];
+  __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int x = wsum[q][lane];
+      int y = x;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, y, off);
+        if (lane >= off) y += v;
+      }
+      wsum[q][lane] = y - x;                             // exclusive over warps
+    }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, to = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = o;
-      s_toff[e] = to;
-      s_tiles[e] = nt;
-      const int c = s_cnt[e];
-      const int n = (c + BN - 1) / BN;
-      o += c;
-      to += n * BN;
-      nt += n;
+  int start[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) start[q] = wsum[q][w] + inc[q] - own[q];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      offsets[e] = start[0];
+      tile_off[e] = start[1];
+      for (int i = 0; i < n[j]; ++i)
+        tiles[start[2] + i] = make_int4(e, start[1] + i * BN, min(BN, c[j] - i * BN), start[0] + i * BN);
     }
-    s_off[E] = o;
-    s_toff[E] = to;
-    s_tiles[E] = nt;
-    *ntiles = nt;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    offsets[e] = s_off[e];
-    tile_off[e] = s_toff[e];
-  }
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int base = s_off[e];
-    for (int b = 0; b < nchunks; ++b) blockcnt[static_cast<size_t>(b) * E + e] += base;
-    const int c = s_cnt[e];
-    for (int i = 0, ti = s_tiles[e]; i * BN < c; ++i, ++ti)
-      tiles[ti] = make_int4(e, s_toff[e] + i * BN, min(BN, c - i * BN), base + i * BN);
+    if (e == E - 1) {                                    // totals
+      offsets[E] = start[0] + c[j];
+      tile_off[E] = start[1] + n[j] * BN;
+      *ntiles = start[2] + n[j];
+    }
+    start[0] += c[j];
+    start[1] += n[j] * BN;
+    start[2] += n[j];
   }
 }
 
@@ -273,7 +314,7 @@ __global__ void __launch_bounds__(32) dispatch_scatter_kernel(const int32_t* __r
   griddep_wait();
   extern __shared__ int32_t pos[];
   const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) pos[e] = blockcnt[static_cast<size_t>(blockIdx.x) * E + e];
+  for (int e = lane; e < E; e += 32) pos[e] = blockcnt[static_cast<size_t>(blockIdx.x) * E + e] + offsets[e];
   __syncwarp();
   const int a0 = blockIdx.x * kDispatchChunk;
   for (int s = 0; s < kDispatchChunk; s += 32) {
@@ -330,8 +371,13 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
     if (e_ != cudaSuccess) return e_;
   }
   {
-    const cudaError_t e_ = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, b.blockcnt,
-                                      nchunks, E, BN, b.counts, b.offsets, b.tile_off, b.tiles, b.ntiles);
+    const cudaError_t e_ = launch_pdl(dispatch_chunkscan_kernel, (E + 7) / 8, 256, 0, s, b.blockcnt, nchunks, E,
+                                      b.counts);
+    if (e_ != cudaSuccess) return e_;
+  }
+  {
+    const cudaError_t e_ = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, static_cast<const int32_t*>(b.counts), E,
+                                      BN, b.offsets, b.tile_off, b.tiles, b.ntiles);
     if (e_ != cudaSuccess) return e_;
   }
   {
