@@ -188,6 +188,30 @@ def cpu_baseline(wl, W_dev, x_dev, ntok=2) -> dict:
             "seconds": dt}
 
 
+# ------------------------------------------------------------- replicas
+# One process per GPU, each a full replica of the layer on its own tokens;
+# the only cross-rank traffic is the barrier and the max of the timings.
+def replica_seeds(wl, rank: int, n: int = 4) -> list:
+    """Seeds of rank `rank`'s n rotating token batches (distinct over ranks)."""
+    return [wl.seed + 7919 * (rank * 8 + i + 1) for i in range(n)]
+
+
+def max_over_ranks(v: float, world: int, device="cuda") -> float:
+    """The slowest rank's value (all ranks get it)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank_step: int, steps: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / seconds
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args):
     import torch
@@ -209,7 +233,7 @@ def run_ours(args):
     wl = C.workload(args.workload)
     T, cfg = wl.T, wl.cfg
     W = G.gen_weights(wl, device="cuda")
-    xs = [G.gen_x(replace(wl, seed=wl.seed + 7919 * (rank * 8 + i + 1)), device="cuda") for i in range(4)]
+    xs = [G.gen_x(replace(wl, seed=sd), device="cuda") for sd in replica_seeds(wl, rank)]
     out = torch.empty(T, cfg.d_model, dtype=torch.bfloat16, device="cuda")
     layer = LatentMoE(cfg, W, max_tokens=T)
     stream = torch.cuda.current_stream()
@@ -250,11 +274,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = clk.stop(t_start, t_end)
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
     prof = layer.lmoe_profile_get()
     n_prof = min(args.steps, 100)
     layer.lmoe_set_profiling(n_prof)
@@ -266,7 +286,7 @@ def run_ours(args):
 
     steps = args.steps
     ms_step = ms / steps
-    value = world * T * steps / (ms / 1e3)
+    value = job_throughput(world, T, steps, ms / 1e3)
     U_mean = sum(U[i % 4] for i in range(steps)) / steps
     pk = peaks()
 
@@ -295,12 +315,8 @@ def run_ours(args):
     t0 = time.perf_counter()
     for i in range(n_e2e):
         layer.lmoe_forward_host(xh[i % 4], oh)
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * T * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * cfg.d_model * 2,
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": job_throughput(world, T, n_e2e, e2e_s), "unit": UNIT, "h2d_bytes_per_step": T * cfg.d_model * 2,
            "d2h_bytes_per_step": T * cfg.d_model * 2, "steps": n_e2e}
 
     cpu = None
