@@ -38,7 +38,7 @@ struct lmoe_ctx {
   size_t pool_bytes = 0;
   int* err = nullptr;
   float* part = nullptr;
-  float* part_sh = nullptr;   // split-K partials of the shared gate/up GEMM (runs on `side`)
+  float* part_sh = nullptr;   // split-K partials of the GEMMs on `side` (latent down, shared gate/up)
   float* xc = nullptr;
   float* logits = nullptr;
   int32_t* idx = nullptr;
@@ -59,11 +59,13 @@ struct lmoe_ctx {
   // static tensor maps
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
   CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
-  // The shared-expert gate/up GEMM does not depend on the routing: it runs on
-  // a side stream forked from the caller's stream at the start of a forward
-  // and joined before the output GEMM that reads h_shared.
+  // The latent down-projection and the shared-expert gate/up GEMM need only
+  // x: they run on a side stream forked from the caller's stream at the start
+  // of a forward, overlapping the router and dispatch; the caller's stream
+  // waits for x^c before encoding the expert inputs (ev_latent) and for
+  // h_shared before the output GEMM (ev_join).
   cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_latent = nullptr, ev_join = nullptr;
   int last_T = 0;
   int last_launches = 0;
   // per-stage event timing
@@ -357,8 +359,9 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     const int nkb_o = ceil_div(h->din, 64) + (h->Fs ? ceil_div(h->Fs, 64) : 0);
     part_elems = std::max(part_elems, max_split_rows(ceil_div(h->d, 128), nkb_o, h->Tm, h->num_sms) * h->d);
   }
-  const long long part_sh_elems =
-      h->Fs ? max_split_rows(2 * ceil_div(h->Fs, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * 2LL * h->Fs : 0;
+  const long long part_sh_elems = std::max(
+      h->Fs ? max_split_rows(2 * ceil_div(h->Fs, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * 2LL * h->Fs : 0LL,
+      h->din ? max_split_rows(ceil_div(h->din, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * h->din : 0LL);
   const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
   const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
@@ -419,15 +422,17 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   auto fail = [&](lmoe_status s) {
     if (h->side) cudaStreamDestroy(h->side);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_latent) cudaEventDestroy(h->ev_latent);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
     cudaFree(h->pool);
     delete h;
     return s;
   };
   if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
-  if (h->Fs && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
-                cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess))
+  if ((h->Fs || h->din) && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+                            cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+                            cudaEventCreateWithFlags(&h->ev_latent, cudaEventDisableTiming) != cudaSuccess ||
+                            cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess))
     return fail(LMOE_ERR_CUDA);
   // expert weights: scale atoms, K padding when a reduction dim is not a multiple of 128
   const uint8_t* sg = static_cast<const uint8_t*>(w->ex_gate_s);
@@ -499,6 +504,7 @@ lmoe_status lmoe_destroy(lmoe_handle h) {
   for (cudaEvent_t ev : h->ev_free) cudaEventDestroy(ev);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_latent) cudaEventDestroy(h->ev_latent);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   cudaFree(h->pool);
   delete h;
@@ -538,12 +544,41 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   const int nt = ceil_div(T, BN);
   const int nkb_d = ceil_div(d, 64);
 
-  // 9 shared experts gate/up + SiTU, on the side stream: it needs only x, so
-  // it overlaps the router, dispatch and routed experts of the caller's stream
-  if (Fs) {
-    cudaStream_t ss = h->side;
+  // Side stream: the steps that need only x overlap the router, dispatch and
+  // routed experts of the caller's stream.
+  cudaStream_t ss = h->side;
+  if (ss) {
     LMOE_TRY(cudaEventRecord(h->ev_fork, st));
     LMOE_TRY(cudaStreamWaitEvent(ss, h->ev_fork, 0));
+  }
+  // 4 latent down-projection (latent layers only)
+  if (din) {
+    StageTimer tm(h, LMOE_STAGE_LATENT_DOWN, ss);
+    DenseParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a0 = h->m_wdown;
+    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
+    p.mode = 0;
+    p.M0 = din;
+    p.mtiles0 = ceil_div(din, 128);
+    p.T = T;
+    p.nkb = nkb_d;
+    p.nkb0 = nkb_d;
+    p.splits = dense_splits(p.mtiles0, nt, nkb_d, h->num_sms);
+    p.ldo = din;
+    p.out = p.splits == 1 ? h->xc : h->part_sh;
+    p.err = h->err;
+    LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, ss));
+    ++launches;
+    if (p.splits > 1) {
+      LMOE_TRY(launch_finalize_sum_f32(h->part_sh, p.splits, T, din, din, h->xc, din, ss));
+      ++launches;
+    }
+    tm.done();
+    LMOE_TRY(cudaEventRecord(h->ev_latent, ss));
+  }
+  // 9 shared experts gate/up + SiTU
+  if (Fs) {
     StageTimer tm(h, LMOE_STAGE_SHARED, ss);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
@@ -578,31 +613,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
   if (s != LMOE_OK) return s;
 
-  // 4 latent down-projection (latent layers only)
-  if (din) {
-    StageTimer tm(h, LMOE_STAGE_LATENT_DOWN, st);
-    DenseParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.a0 = h->m_wdown;
-    if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
-    p.mode = 0;
-    p.M0 = din;
-    p.mtiles0 = ceil_div(din, 128);
-    p.T = T;
-    p.nkb = nkb_d;
-    p.nkb0 = nkb_d;
-    p.splits = dense_splits(p.mtiles0, nt, nkb_d, h->num_sms);
-    p.ldo = din;
-    p.out = p.splits == 1 ? h->xc : h->part;
-    p.err = h->err;
-    LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
-    ++launches;
-    if (p.splits > 1) {
-      LMOE_TRY(launch_finalize_sum_f32(h->part, p.splits, T, din, din, h->xc, din, st));
-      ++launches;
-    }
-    tm.done();
-  }
+  if (din) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_latent, 0));   // x^c from the side stream
   // 5 activations -> hi/lo E4M3 in expert-tile order
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
