@@ -99,14 +99,16 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
   __shared__ int32_t hist[kMaxExperts];
   __shared__ int32_t s_off[kMaxExperts + 1];
   __shared__ int32_t s_toff[kMaxExperts + 1];
-  __shared__ int32_t s_tst[kMaxExperts + 1];
   __shared__ int32_t wsum[3][32];
+  extern __shared__ int16_t s_idx[];                     // [P] expert ids, -1 for an invalid id
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   for (int a = tid; a < P; a += blockDim.x) {
     const int e = idx[a];
-    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    const bool ok = e >= 0 && e < E;
+    s_idx[a] = static_cast<int16_t>(ok ? e : -1);
+    if (ok) atomicAdd(&hist[e], 1);
     else if (err) atomicExch(err + 1, 1);
   }
   __syncthreads();
@@ -153,7 +155,6 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
     if (e < E) {
       s_off[e] = base[0];
       s_toff[e] = base[1];
-      s_tst[e] = base[2];
       counts[e] = v[q][0];
       offsets[e] = base[0];
       tile_off[e] = base[1];
@@ -172,8 +173,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(const int32_t* __r
   if (warp == 0) {
     for (int a0 = 0; a0 < P; a0 += 32) {
       const int a = a0 + lane;
-      int e = a < P ? idx[a] : -1;
-      if (e < 0 || e >= E) e = -1;
+      const int e = a < P ? s_idx[a] : -1;
       const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       const int b = e >= 0 ? s_off[e] : 0;
@@ -356,7 +356,8 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
   if (P <= 0) return cudaSuccess;
   if (P <= kSmallDispatch) {
     {
-      const cudaError_t e_ = launch_pdl(dispatch_small_kernel, 1, 1024, 0, s, idx,
+      const size_t smem = static_cast<size_t>(P) * sizeof(int16_t);   // staged expert ids
+      const cudaError_t e_ = launch_pdl(dispatch_small_kernel, 1, 1024, smem, s, idx,
                                         P, E, BN, b.counts, b.offsets, b.perm, b.inv_pad, b.tile_off, b.tiles,
                                         b.ntiles, b.err);
       if (e_ != cudaSuccess) return e_;
