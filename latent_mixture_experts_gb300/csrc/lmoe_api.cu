@@ -47,7 +47,7 @@ struct lmoe_ctx {
   int32_t *blockcnt = nullptr, *ntiles = nullptr;
   int4* tiles = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr;
-  float* y = nullptr;
+  __nv_bfloat16* y = nullptr;   // per-assignment G-scaled expert outputs
   float* u = nullptr;
   void* u_hat = nullptr;
   void* h_s = nullptr;
@@ -390,7 +390,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->xsf = c.take<uint8_t>(xsf_bytes, base);
     h->hq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Fp, base);
     h->hsf = c.take<uint8_t>(hsf_bytes, base);
-    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->dx, base);
+    h->y = c.take<__nv_bfloat16>(static_cast<size_t>(h->Pm) * h->dx, base);
     h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);

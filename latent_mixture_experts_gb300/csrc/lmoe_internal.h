@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cstdint>
 
 namespace lmoe {
@@ -151,7 +152,7 @@ struct MoeGemmParams {
   int act;
   float b1, b2;
   // down epilogue
-  float* y;                      // [T*k][din] fp32, G-scaled expert outputs
+  __nv_bfloat16* y;              // [T*k][dx] bf16, G-scaled expert outputs (summed in fp32 by the combine)
   // FP8 weights: fp32 scale per 128 x 128 block, [E][NB][KB]; wsc1 = up scales (gate/up pass)
   const float* wsc0;
   const float* wsc1;
@@ -165,8 +166,8 @@ cudaError_t launch_moe_fp8_down(const MoeGemmParams& p, int BN, int grid, cudaSt
 cudaError_t launch_dequant_fp8_block128(const uint8_t* q, const float* s, int N, int K, void* out, cudaStream_t st);
 
 // u[t] = sum_j y[t*k + j] (slot order); u_hat = w * u / sqrt(mean(u^2) + eps) -> bf16.
-cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
-                                float* u, void* u_hat, cudaStream_t s);
+cudaError_t launch_combine_norm(const __nv_bfloat16* y, int T, int k, int l, const void* norm_w, int use_norm,
+                                float eps, float* u, void* u_hat, cudaStream_t s);
 
 // Create-time repacking of the expert weights.
 cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,

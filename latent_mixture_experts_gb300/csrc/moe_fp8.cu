@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
             if (c_base + j < nrows) {
               const int a = __shfl_sync(0xFFFFFFFFu, a_l[j / 32], j % 32);
               const float gw = __shfl_sync(0xFFFFFFFFu, g_l[j / 32], j % 32);
-              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = acc[i][j] * gw;
+              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __float2bfloat16_rn(acc[i][j] * gw);
             }
           }
         }
