@@ -15,19 +15,23 @@ namespace lmoe {
 
 namespace {
 
-template <int BN>
+// MT: 128-row weight tiles per CTA.  MT = 2 (wide, prefill-sized BN = 256):
+// one 256-row A box per stage and two accumulators filling tensor memory,
+// which halves the activation bytes each CTA moves per MAC.
+template <int BN, int MT>
 struct DenseCfg {
-  static constexpr int kA = 16384;             // 128 rows x 64 bf16
+  static constexpr int kA = MT * 16384;        // MT x 128 rows x 64 bf16
   static constexpr int kB = BN * 128;          // BN rows x 64 bf16
   static constexpr int kStage = kA + kB;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 5 : 6);
+  static constexpr int kStages = MT == 2 ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 5 : 6));
   static constexpr int kSmem = kStages * kStage + 1024;
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr int kTmemCols = MT * BN < 32 ? 32 : MT * BN;
+  static_assert(kTmemCols <= 512, "tensor memory budget");
 };
 
-template <int BN>
+template <int BN, int MT>
 __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constant__ DenseParams p) {
-  using C = DenseCfg<BN>;
+  using C = DenseCfg<BN, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   __shared__ uint64_t full[C::kStages], empty[C::kStages], done;
@@ -35,8 +39,9 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, nt = blockIdx.y, sp = blockIdx.z;
-  const int seg = (p.mode == 1 && mt >= p.mtiles0) ? 1 : 0;
-  const int m0 = (seg ? mt - p.mtiles0 : mt) * 128;
+  const int mtw0 = (p.mtiles0 + MT - 1) / MT;           // CTA tiles of the first segment
+  const int seg = (p.mode == 1 && mt >= mtw0) ? 1 : 0;
+  const int m0 = (seg ? mt - mtw0 : mt) * 128 * MT;
   const int Mseg = seg ? p.M1 : p.M0;
   const int out_row0 = (seg ? p.M0 : 0) + m0;
   const int n0 = nt * BN;
@@ -64,7 +69,7 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
 
   if (warp == 0 && lane == 0) {
     // TMA producer
-    const CUtensorMap* am = seg ? &p.a1 : &p.a0;
+    const CUtensorMap* am = MT == 2 ? (seg ? &p.a1w : &p.a0w) : (seg ? &p.a1 : &p.a0);
     tma_prefetch_desc(am);
     tma_prefetch_desc(&p.b0);
     for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
@@ -74,7 +79,7 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
       const CUtensorMap* B = &p.b0;
       int kc = kb * 64;
       if (p.mode == 2 && kb >= p.nkb0) {
-        A = &p.a1;
+        A = MT == 2 ? &p.a1w : &p.a1;
         B = &p.b1;
         kc = (kb - p.nkb0) * 64;
       }
@@ -94,7 +99,10 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
       const uint32_t b_addr = a_addr + C::kA;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_bf16(tacc, sdesc_sw128(a_addr + 32 * k), sdesc_sw128(b_addr + 32 * k), idesc, (i | k) != 0);
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+          mma_bf16(tacc + t * BN, sdesc_sw128(a_addr + t * 16384 + 32 * k), sdesc_sw128(b_addr + 32 * k), idesc,
+                   (i | k) != 0);
       mma_commit(&empty[s]);
     }
     mma_commit(&done);
@@ -104,21 +112,24 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   // Epilogue: lane = output feature, column = token.
   const bool ok = mbar_wait(&done, 0, p.err, kErrTimeout);
   tc_fence_after();
-  const int row = m0 + 32 * warp + lane;
-  const bool row_ok = row < Mseg;
   const bool have = ok && kb1 > kb0;
-  float* outp = p.out + static_cast<size_t>(sp) * p.T * p.ldo + out_row0 + 32 * warp + lane;
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 16) {
-    if (n0 + c0 >= p.T) break;
-    uint32_t r[16];
-    tmem_ld16(tmem_addr(tacc, 32 * warp, c0), r);
-    tmem_ld_wait();
-    if (row_ok) {
+  for (int mtl = 0; mtl < MT; ++mtl) {
+    const int row = m0 + mtl * 128 + 32 * warp + lane;
+    const bool row_ok = row < Mseg;
+    float* outp = p.out + static_cast<size_t>(sp) * p.T * p.ldo + out_row0 + mtl * 128 + 32 * warp + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      if (n0 + c0 >= p.T) break;
+      uint32_t r[16];
+      tmem_ld16(tmem_addr(tacc + mtl * BN, 32 * warp, c0), r);
+      tmem_ld_wait();
+      if (row_ok) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int t = n0 + c0 + j;
-        if (t < p.T) outp[static_cast<size_t>(t) * p.ldo] = have ? __uint_as_float(r[j]) : 0.0f;
+        for (int j = 0; j < 16; ++j) {
+          const int t = n0 + c0 + j;
+          if (t < p.T) outp[static_cast<size_t>(t) * p.ldo] = have ? __uint_as_float(r[j]) : 0.0f;
+        }
       }
     }
   }
@@ -127,18 +138,22 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   if (warp == 0) tmem_dealloc(tacc, C::kTmemCols);
 }
 
-template <int BN>
+template <int BN, int MT>
 cudaError_t launch_bn(const DenseParams& p, int mtiles, cudaStream_t s) {
-  using C = DenseCfg<BN>;
+  using C = DenseCfg<BN, MT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dense_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(dense_gemm_kernel<BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(mtiles, (p.T + BN - 1) / BN, p.splits);
+  // CTA tiles: MT 128-row tiles each, counted per M segment
+  const int seg0 = p.mode == 1 ? p.mtiles0 : mtiles;
+  const int ctas_m = (seg0 + MT - 1) / MT + (mtiles - seg0 + MT - 1) / MT;
+  dim3 grid(ctas_m, (p.T + BN - 1) / BN, p.splits);
   {
-    const cudaError_t e_ = launch_pdl(dense_gemm_kernel<BN>, grid, 128, C::kSmem, s, p);
+    const cudaError_t e_ = launch_pdl(dense_gemm_kernel<BN, MT>, grid, 128, C::kSmem, s, p);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
@@ -204,10 +219,10 @@ int ew_grid(size_t n) {
 
 cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s) {
   switch (BN) {
-    case 32: return launch_bn<32>(p, mtiles, s);
-    case 64: return launch_bn<64>(p, mtiles, s);
-    case 128: return launch_bn<128>(p, mtiles, s);
-    case 256: return launch_bn<256>(p, mtiles, s);
+    case 32: return launch_bn<32, 1>(p, mtiles, s);
+    case 64: return launch_bn<64, 1>(p, mtiles, s);
+    case 128: return launch_bn<128, 1>(p, mtiles, s);
+    case 256: return p.wide ? launch_bn<256, 2>(p, mtiles, s) : launch_bn<256, 1>(p, mtiles, s);
     default: return cudaErrorInvalidValue;
   }
 }

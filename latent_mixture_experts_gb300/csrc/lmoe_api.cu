@@ -58,6 +58,7 @@ struct lmoe_ctx {
   uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
   // static tensor maps
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
+  CUtensorMap m_routerw, m_wdownw, m_wupw, m_shgw, m_shuw, m_shdw;   // 256-row boxes (wide dense tiles)
   CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
   // The latent down-projection and the shared-expert gate/up GEMM need only
   // x: they run on a side stream forked from the caller's stream at the start
@@ -101,6 +102,13 @@ int expert_bn(const lmoe_ctx* h, int T) {
 
 // K splits of a dense GEMM: fill about one wave of CTAs, at least two
 // 64-wide k-blocks per split.
+// A dense GEMM runs wide (two 128-row weight tiles per CTA) at the prefill
+// token tile when it needs no K split and the paired tiles still fill the SMs.
+int dense_wide(int BN, int splits, int mtiles_seg0, int mtiles_seg1, int nt, int num_sms) {
+  if (BN != 256 || splits != 1) return 0;
+  return ((mtiles_seg0 + 1) / 2 + (mtiles_seg1 + 1) / 2) * nt >= num_sms ? 1 : 0;
+}
+
 int dense_splits(int mtiles, int ntiles, int nkb, int num_sms) {
   const int tiles = mtiles * ntiles;
   int s = num_sms / std::max(tiles, 1);
@@ -203,6 +211,7 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
   DenseParams p;
   std::memset(&p, 0, sizeof(p));
   p.a0 = h->m_router;
+  p.a0w = h->m_routerw;
   if (!map_bf16(&p.b0, x, h->d, T, BN)) return LMOE_ERR_CUDA;
   p.mode = 0;
   p.M0 = h->E;
@@ -211,6 +220,7 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
   p.nkb = ceil_div(h->d, 64);
   p.nkb0 = p.nkb;
   p.splits = dense_splits(p.mtiles0, ceil_div(T, BN), p.nkb, h->num_sms);
+  p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, ceil_div(T, BN), h->num_sms);
   p.ldo = h->E;
   p.out = h->part;
   p.err = h->err;
@@ -478,6 +488,16 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     ok &= map_bf16(&h->m_shu, sh16 ? h->sh_u16 : w->sh_up, h->d, h->Fs, 128);
     ok &= map_bf16(&h->m_shd, sh16 ? h->sh_d16 : w->sh_down, h->Fs, h->d, 128);
   }
+  ok &= map_bf16(&h->m_routerw, w->router_w, h->d, h->E, 256);
+  if (h->din) {
+    ok &= map_bf16(&h->m_wdownw, w->w_down_latent, h->d, h->din, 256);
+    ok &= map_bf16(&h->m_wupw, w->w_up_latent, h->din, h->d, 256);
+  }
+  if (h->Fs) {
+    ok &= map_bf16(&h->m_shgw, sh16 ? h->sh_g16 : w->sh_gate, h->d, h->Fs, 256);
+    ok &= map_bf16(&h->m_shuw, sh16 ? h->sh_u16 : w->sh_up, h->d, h->Fs, 256);
+    ok &= map_bf16(&h->m_shdw, sh16 ? h->sh_d16 : w->sh_down, h->Fs, h->d, 256);
+  }
   for (int i = 0; i < 2; ++i) {
     const int rows = 128 << i;
     if (h->fp8) {
@@ -557,6 +577,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_wdown;
+    p.a0w = h->m_wdownw;
     if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
     p.mode = 0;
     p.M0 = din;
@@ -565,6 +586,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.nkb = nkb_d;
     p.nkb0 = nkb_d;
     p.splits = dense_splits(p.mtiles0, nt, nkb_d, h->num_sms);
+    p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
     p.ldo = din;
     p.out = p.splits == 1 ? h->xc : h->part_sh;
     p.err = h->err;
@@ -584,6 +606,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_shg;
     p.a1 = h->m_shu;
+    p.a0w = h->m_shgw;
+    p.a1w = h->m_shuw;
     if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
     p.mode = 1;
     p.M0 = Fs;
@@ -593,6 +617,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.nkb = nkb_d;
     p.nkb0 = nkb_d;
     p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
+    p.wide = dense_wide(BN, p.splits, p.mtiles0, p.mtiles0, nt, h->num_sms);
     p.ldo = 2 * Fs;
     p.out = h->part_sh;
     p.err = h->err;
@@ -696,6 +721,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_wup;
+    p.a0w = h->m_wupw;
     if (!map_bf16(&p.b0, h->u_hat, din, T, BN)) return LMOE_ERR_CUDA;
     p.nkb0 = ceil_div(din, 64);
     p.nkb = p.nkb0;
@@ -703,6 +729,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     if (Fs) {
       p.mode = 2;
       p.a1 = h->m_shd;
+      p.a1w = h->m_shdw;
       if (!map_bf16(&p.b1, h->h_s, Fs, T, BN)) return LMOE_ERR_CUDA;
       p.nkb += ceil_div(Fs, 64);
     }
@@ -710,6 +737,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.mtiles0 = ceil_div(d, 128);
     p.T = T;
     p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
+    p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
     p.ldo = d;
     p.out = h->part;
     p.err = h->err;
@@ -725,6 +753,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
       DenseParams p;
       std::memset(&p, 0, sizeof(p));
       p.a0 = h->m_shd;
+      p.a0w = h->m_shdw;
       if (!map_bf16(&p.b0, h->h_s, Fs, T, BN)) return LMOE_ERR_CUDA;
       p.mode = 0;
       p.nkb0 = ceil_div(Fs, 64);
@@ -733,6 +762,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
       p.mtiles0 = ceil_div(d, 128);
       p.T = T;
       p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
+      p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
       p.ldo = d;
       p.out = h->part;
       p.err = h->err;

@@ -22,6 +22,8 @@ constexpr int kMaxExperts = 2048;
 //           (K concatenation, one accumulator).
 struct DenseParams {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap a0w, a1w;   // the same weights with 256-row boxes (used when wide)
+  int wide;               // 1: each CTA computes 256 weight rows (two accumulators), BN = 256, splits = 1
   float* out;
   int* err;
   int mode;
@@ -31,7 +33,8 @@ struct DenseParams {
   int splits;
   int ldo;
 };
-// BN: token tile (32, 64, 128 or 256).  Grid (mtiles, ceil(T/BN), splits).
+// BN: token tile (32, 64, 128 or 256).  Grid (mtiles, ceil(T/BN), splits);
+// mtiles and mtiles0 count 128-row tiles (a wide launch pairs them).
 cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s);
 
 // Sum `splits` partial planes [splits][T][ld] and apply an epilogue.

@@ -51,3 +51,30 @@ def test_all_token_tiles(wl, Ts):
         assert torch.equal(a, b)
     finally:
         layer.close()
+
+
+# d = 1024, Fs = 1024 at T = 10,000 (40 tiles of 256 tokens): the shared
+# gate/up GEMM (2 x 4 paired weight tiles) and the K-concatenated output GEMM
+# (4 paired tiles) run wide, two 128-row accumulators per CTA, while the
+# router and the latent GEMM keep one tile per CTA.
+WIDE = C.Workload("k3_wide_dense", replace(C.K3_TINY, d_model=1024, d_latent=512, n_experts=32, top_k=2,
+                                           d_expert_ff=256, d_shared_ff=1024), T=10000, seed=54)
+
+
+def test_wide_dense_tiles_all_tokens():
+    wl = WIDE
+    W, x = gpu_inputs(wl)
+    layer = make_layer(wl, W, max_tokens=wl.T)
+    olayer = oracle_layer(wl, W)
+    try:
+        out, idx, _ = layer.lmoe_forward(x, return_routing=True)
+        torch.cuda.synchronize()
+        layer.lmoe_sync_status()
+        idx = idx.cpu().numpy()
+        ref = O.forward(olayer, x_bits(x), idx=idx)
+        hs = layer.lmoe_debug_tensor("h_shared", wl.T).cpu().double().numpy()
+        assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
+        rel, beyond = assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+        print(f"{wl.name} T={wl.T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
+    finally:
+        layer.close()
