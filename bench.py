@@ -90,7 +90,7 @@ def accounting(cfg) -> dict:
     act_in = 2 * din + 2 * din // 32
     h_io = 2 * F + 2 * F // 32
     return dict(din=din, gu_w=gu_w, dn_w=dn_w, expert=gu_w + dn_w, dense=dense, token_io=2 * d * 2,
-                flops_per_token=flops, gu_per_assign=act_in + h_io, dn_per_assign=h_io + din * 2)
+                flops_per_token=flops, gu_per_assign=act_in + h_io, dn_per_assign=h_io + din * 4)
 
 
 def peaks():

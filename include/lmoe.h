@@ -183,8 +183,11 @@ LMOE_API lmoe_status lmoe_dispatch_noalloc(const int32_t* topk_idx, int T, int k
  * workspace (stream-ordered): "logits" fp32 [T][E] (router z), "xc" fp32
  * [T][l], "u" fp32 [T][l] (expert sum; [T][d] for non-latent layers, where
  * it is y_routed), "u_hat" bf16 [T][l] (latent layers), "h_shared"
- * bf16 [T][Fs], "counts" int32 [E], "offsets" int32 [E+1], "perm" int32
- * [T*k].  `bytes` must equal the tensor's size for the last T. */
+ * bf16 [T][Fs] (layers with a bf16 shared MLP), "y_shared" fp32 [T][d]
+ * (FP8 layers, whose shared expert runs on the FP8 expert GEMMs), "counts"
+ * int32 [E], "offsets" int32 [E+1], "perm" int32 [T*k].  `bytes` must
+ * equal the tensor's size for the last T; a name the layer does not have
+ * returns INVALID_ARG. */
 LMOE_API lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t stream);
 
 /* Synchronise `stream` and return the first deferred error: a CUDA error, a

@@ -201,7 +201,8 @@ class LatentMoE:
         dx = c.d_latent or c.d_model          # width of the expert sum (the latent, or d for K2-style layers)
         shapes = {"logits": ((T, c.n_experts), torch.float32), "xc": ((T, c.d_latent), torch.float32),
                   "u": ((T, dx), torch.float32), "u_hat": ((T, dx), torch.bfloat16),
-                  "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "counts": ((c.n_experts,), torch.int32),
+                  "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "y_shared": ((T, c.d_model), torch.float32),
+                  "counts": ((c.n_experts,), torch.int32),
                   "offsets": ((c.n_experts + 1,), torch.int32), "perm": ((T * c.top_k,), torch.int32)}
         shape, dt = shapes[name]
         dst = torch.empty(shape, dtype=dt, device="cuda")

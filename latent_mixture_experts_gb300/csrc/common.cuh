@@ -49,13 +49,17 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
 // 2^(e - 127) for an E8M0 byte e in [1, 254], built from its bit pattern.
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e) { return __uint_as_float(e << 23); }
 
-// E8M0 scale byte for a 32-element block whose largest magnitude is amax,
-// chosen so that amax / scale lands in [256, 512): the top binade of E4M3
-// (largest finite 448; values above it saturate).  Clamped so the scale and
-// its reciprocal stay normal floats.
+// E8M0 scale byte for a 32-element block whose largest magnitude is amax:
+// the smallest power of two with amax / scale <= 448, the largest finite
+// E4M3.  With s = exponent(amax) - 8, amax / scale = 256 * (1 + mantissa),
+// which passes 448 once the mantissa exceeds 0.75; such a block takes the
+// next scale up (amax / scale in (224, 256]) so that no code saturates —
+// a saturated hi code leaves a residual the lo term, scaled the same way,
+// cannot hold either.  Clamped so the scale and its reciprocal stay normal.
 __device__ __forceinline__ uint32_t e4m3_block_scale(float amax) {
-  const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
-  int s = ef - 8;
+  const uint32_t bits = __float_as_uint(amax);
+  const int ef = static_cast<int>((bits >> 23) & 0xFF);
+  int s = ef - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
   s = s < 1 ? 1 : (s > 253 ? 253 : s);
   return static_cast<uint32_t>(s);
 }

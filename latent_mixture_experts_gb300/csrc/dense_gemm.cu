@@ -40,8 +40,9 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, nt = blockIdx.y, sp = blockIdx.z;
   const int mtw0 = (p.mtiles0 + MT - 1) / MT;           // CTA tiles of the first segment
-  const int seg = (p.mode == 1 && mt >= mtw0) ? 1 : 0;
-  const int m0 = (seg ? mt - mtw0 : mt) * 128 * MT;
+  const bool pair = MT == 2 && p.epi == 2;               // gate rows + up rows of the same features
+  const int seg = (!pair && p.mode == 1 && mt >= mtw0) ? 1 : 0;
+  const int m0 = pair ? mt * 128 : (seg ? mt - mtw0 : mt) * 128 * MT;
   const int Mseg = seg ? p.M1 : p.M0;
   const int out_row0 = (seg ? p.M0 : 0) + m0;
   const int n0 = nt * BN;
@@ -85,7 +86,12 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
       }
       uint8_t* st = sm + s * C::kStage;
       mbar_arrive_expect_tx(&full[s], C::kStage);
-      tma_load_2d(st, A, &full[s], kc, m0);
+      if (pair) {
+        tma_load_2d(st, &p.a0, &full[s], kc, m0);
+        tma_load_2d(st + 16384, &p.a1, &full[s], kc, m0);
+      } else {
+        tma_load_2d(st, A, &full[s], kc, m0);
+      }
       tma_load_2d(st + C::kA, B, &full[s], kc, n0);
     }
   } else if (warp == 1 && lane == 0) {
@@ -113,8 +119,30 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   const bool ok = mbar_wait(&done, 0, p.err, kErrTimeout);
   tc_fence_after();
   const bool have = ok && kb1 > kb0;
+  if (pair) {
+    // h[t][f] = act(gate, up): gate in the first accumulator, up in the second
+    const int f = m0 + 32 * warp + lane;
+    __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(p.out16);
 #pragma unroll 1
-  for (int mtl = 0; mtl < MT; ++mtl) {
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      if (n0 + c0 >= p.T) break;
+      uint32_t g[16], u[16];
+      tmem_ld16(tmem_addr(tacc, 32 * warp, c0), g);
+      tmem_ld16(tmem_addr(tacc + BN, 32 * warp, c0), u);
+      tmem_ld_wait();
+      if (f < p.M0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = n0 + c0 + j;
+          const float h =
+              have ? glu_act(__uint_as_float(g[j]), __uint_as_float(u[j]), p.act, p.act_b1, p.act_b2) : 0.0f;
+          if (t < p.T) o16[static_cast<size_t>(t) * p.ldo + f] = __float2bfloat16_rn(h);
+        }
+      }
+    }
+  }
+#pragma unroll 1
+  for (int mtl = 0; mtl < (pair ? 0 : MT); ++mtl) {
     const int row = m0 + mtl * 128 + 32 * warp + lane;
     const bool row_ok = row < Mseg;
     float* outp = p.out + static_cast<size_t>(sp) * p.T * p.ldo + out_row0 + mtl * 128 + 32 * warp + lane;
@@ -124,7 +152,20 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
       uint32_t r[16];
       tmem_ld16(tmem_addr(tacc + mtl * BN, 32 * warp, c0), r);
       tmem_ld_wait();
-      if (row_ok) {
+      if (row_ok && p.epi == 1) {
+        // direct bf16 result (one K split), plus the optional fp32 addend
+        __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(p.out16) + out_row0 + mtl * 128 + 32 * warp + lane;
+        const float* ad = p.add ? p.add + out_row0 + mtl * 128 + 32 * warp + lane : nullptr;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = n0 + c0 + j;
+          if (t < p.T) {
+            float v = have ? __uint_as_float(r[j]) : 0.0f;
+            if (ad) v += ad[static_cast<size_t>(t) * p.ld_add];
+            o16[static_cast<size_t>(t) * p.ldo] = __float2bfloat16_rn(v);
+          }
+        }
+      } else if (row_ok) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = n0 + c0 + j;
@@ -148,9 +189,11 @@ cudaError_t launch_bn(const DenseParams& p, int mtiles, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // CTA tiles: MT 128-row tiles each, counted per M segment
+  // CTA tiles: MT 128-row tiles each, counted per M segment (a gate/up pair
+  // CTA covers one 128-row tile of each segment)
   const int seg0 = p.mode == 1 ? p.mtiles0 : mtiles;
-  const int ctas_m = (seg0 + MT - 1) / MT + (mtiles - seg0 + MT - 1) / MT;
+  const int ctas_m = (MT == 2 && p.epi == 2) ? p.mtiles0
+                                             : (seg0 + MT - 1) / MT + (mtiles - seg0 + MT - 1) / MT;
   dim3 grid(ctas_m, (p.T + BN - 1) / BN, p.splits);
   {
     const cudaError_t e_ = launch_pdl(dense_gemm_kernel<BN, MT>, grid, 128, C::kSmem, s, p);

@@ -30,7 +30,14 @@ struct lmoe_ctx {
   int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
   int dx = 0;          // width the routed experts read and write: the latent, or d for non-latent layers
   bool fp8 = false;    // experts in FP8 E4M3 with 128 x 128 fp32 block scales
-  void *sh_g16 = nullptr, *sh_u16 = nullptr, *sh_d16 = nullptr;   // bf16 copies of an FP8 shared expert
+  // FP8 layers run the shared expert on the FP8 expert GEMMs, as one expert
+  // that every token uses (exact block-scaled weights): its tile list, identity
+  // rows and unit weights, hi/lo activations and its fp32 output.
+  int4* sh_tiles = nullptr;
+  int32_t *sh_tile_off = nullptr, *sh_ntiles = nullptr, *sh_iota = nullptr;
+  float *sh_ones = nullptr, *y_sh = nullptr;
+  uint8_t *xq_sh = nullptr, *xsf_sh = nullptr, *hq_sh = nullptr, *hsf_sh = nullptr;
+  int Tpad_sh = 0;
   int Kp = 0, Fp = 0, MT_gu = 0, MT_dn = 0, KG_gu = 0, KG_dn = 0, MTa_gu = 0, MTa_dn = 0;
   int Tm = 0, Pm = 0, Ppad = 0, max_tiles = 0, nchunks_max = 0;
   // device memory
@@ -47,7 +54,7 @@ struct lmoe_ctx {
   int32_t *blockcnt = nullptr, *ntiles = nullptr;
   int4* tiles = nullptr;
   uint8_t *xq = nullptr, *xsf = nullptr, *hq = nullptr, *hsf = nullptr;
-  __nv_bfloat16* y = nullptr;   // per-assignment G-scaled expert outputs
+  float* y = nullptr;           // per-assignment G-scaled expert outputs
   float* u = nullptr;
   void* u_hat = nullptr;
   void* h_s = nullptr;
@@ -60,6 +67,7 @@ struct lmoe_ctx {
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
   CUtensorMap m_routerw, m_wdownw, m_wupw, m_shgw, m_shuw, m_shdw;   // 256-row boxes (wide dense tiles)
   CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
+  CUtensorMap m_sg, m_su, m_sd;               // FP8 shared-expert codes, 128-row boxes
   // The latent down-projection and the shared-expert gate/up GEMM need only
   // x: they run on a side stream forked from the caller's stream at the start
   // of a forward, overlapping the router and dispatch; the caller's stream
@@ -261,7 +269,7 @@ lmoe_status validate_cfg(const lmoe_config* c) {
   if (c->expert_wfmt == LMOE_W_MXFP4 && c->d_latent == 0) return LMOE_ERR_UNSUPPORTED;
   if (c->expert_wfmt == LMOE_W_FP8_BLOCK128 &&
       (c->d_latent != 0 || c->use_latent_norm || c->d_model % 128 || c->d_expert_ff % 128 || c->d_shared_ff % 128 ||
-       c->d_model > kFp8MaxK || c->d_expert_ff > kFp8MaxK))
+       c->d_model > kFp8MaxK || c->d_expert_ff > kFp8MaxK || c->d_shared_ff > kFp8MaxK))
     return LMOE_ERR_UNSUPPORTED;
   if (c->d_model % 32 || c->d_latent % 32 || c->d_expert_ff % 32 || c->d_shared_ff % 32) return LMOE_ERR_UNSUPPORTED;
   if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
@@ -377,7 +385,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
   const size_t sfa_gu_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512;
   const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512;
-  const bool sh16 = h->fp8 && h->Fs;
+  const bool sh8 = h->fp8 && h->Fs;   // shared expert on the FP8 expert GEMMs
+  h->Tpad_sh = sh8 ? h->Tm + kFp8MaxTile : 0;
 
   auto carve = [&](char* base) {
     Carve c;
@@ -400,7 +409,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->xsf = c.take<uint8_t>(xsf_bytes, base);
     h->hq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Fp, base);
     h->hsf = c.take<uint8_t>(hsf_bytes, base);
-    h->y = c.take<__nv_bfloat16>(static_cast<size_t>(h->Pm) * h->dx, base);
+    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->dx, base);
     h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);
@@ -409,10 +418,18 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->sfa_gate = c.take<uint8_t>(sfa_gu_bytes, base);
     h->sfa_up = c.take<uint8_t>(sfa_gu_bytes, base);
     h->sfa_down = c.take<uint8_t>(sfa_dn_bytes, base);
-    if (sh16) {
-      h->sh_g16 = c.take<uint16_t>(static_cast<size_t>(h->Fs) * h->d, base);
-      h->sh_u16 = c.take<uint16_t>(static_cast<size_t>(h->Fs) * h->d, base);
-      h->sh_d16 = c.take<uint16_t>(static_cast<size_t>(h->d) * h->Fs, base);
+    if (sh8) {
+      const size_t tiles_max = static_cast<size_t>(h->Tpad_sh / 16 + 1);
+      h->sh_tiles = c.take<int4>(tiles_max, base);
+      h->sh_tile_off = c.take<int32_t>(2, base);
+      h->sh_ntiles = c.take<int32_t>(1, base);
+      h->sh_iota = c.take<int32_t>(h->Tm, base);
+      h->sh_ones = c.take<float>(h->Tm, base);
+      h->xq_sh = c.take<uint8_t>(2 * static_cast<size_t>(h->Tpad_sh) * h->d, base);
+      h->xsf_sh = c.take<uint8_t>(tiles_max * (h->d / 128) * 1024, base);
+      h->hq_sh = c.take<uint8_t>(2 * static_cast<size_t>(h->Tpad_sh) * h->Fs, base);
+      h->hsf_sh = c.take<uint8_t>(tiles_max * (h->Fs / 128) * 1024, base);
+      h->y_sh = c.take<float>(static_cast<size_t>(h->Tm) * h->d, base);
     }
     if (pad_gu) {
       h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
@@ -453,15 +470,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
        launch_relayout_sfa(su, h->E, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
        launch_relayout_sfa(sd, h->E, h->dx, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess))
     return fail(LMOE_ERR_CUDA);
-  // FP8 shared expert: one bf16 copy at create (0.26% of a K2 layer's bytes), then the bf16 GEMMs
-  if (sh16 &&
-      (launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_gate), static_cast<const float*>(w->sh_gate_s),
-                                   h->Fs, h->d, h->sh_g16, stream) != cudaSuccess ||
-       launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_up), static_cast<const float*>(w->sh_up_s),
-                                   h->Fs, h->d, h->sh_u16, stream) != cudaSuccess ||
-       launch_dequant_fp8_block128(static_cast<const uint8_t*>(w->sh_down), static_cast<const float*>(w->sh_down_s),
-                                   h->d, h->Fs, h->sh_d16, stream) != cudaSuccess))
-    return fail(LMOE_ERR_CUDA);
+  if (sh8 && launch_iota_ones(h->sh_iota, h->sh_ones, h->Tm, stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
   h->codes_gate = w->ex_gate_q;
   h->codes_up = w->ex_up_q;
   h->codes_down = w->ex_down_q;
@@ -483,20 +492,25 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     ok &= map_bf16(&h->m_wdown, w->w_down_latent, h->d, h->din, 128);
     ok &= map_bf16(&h->m_wup, w->w_up_latent, h->din, h->d, 128);
   }
-  if (h->Fs) {
-    ok &= map_bf16(&h->m_shg, sh16 ? h->sh_g16 : w->sh_gate, h->d, h->Fs, 128);
-    ok &= map_bf16(&h->m_shu, sh16 ? h->sh_u16 : w->sh_up, h->d, h->Fs, 128);
-    ok &= map_bf16(&h->m_shd, sh16 ? h->sh_d16 : w->sh_down, h->Fs, h->d, 128);
+  if (h->Fs && !sh8) {
+    ok &= map_bf16(&h->m_shg, w->sh_gate, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shu, w->sh_up, h->d, h->Fs, 128);
+    ok &= map_bf16(&h->m_shd, w->sh_down, h->Fs, h->d, 128);
+  }
+  if (sh8) {
+    ok &= map_u8(&h->m_sg, w->sh_gate, h->d, h->Fs, kFp8Rows);
+    ok &= map_u8(&h->m_su, w->sh_up, h->d, h->Fs, kFp8Rows);
+    ok &= map_u8(&h->m_sd, w->sh_down, h->Fs, h->d, kFp8Rows);
   }
   ok &= map_bf16(&h->m_routerw, w->router_w, h->d, h->E, 256);
   if (h->din) {
     ok &= map_bf16(&h->m_wdownw, w->w_down_latent, h->d, h->din, 256);
     ok &= map_bf16(&h->m_wupw, w->w_up_latent, h->din, h->d, 256);
   }
-  if (h->Fs) {
-    ok &= map_bf16(&h->m_shgw, sh16 ? h->sh_g16 : w->sh_gate, h->d, h->Fs, 256);
-    ok &= map_bf16(&h->m_shuw, sh16 ? h->sh_u16 : w->sh_up, h->d, h->Fs, 256);
-    ok &= map_bf16(&h->m_shdw, sh16 ? h->sh_d16 : w->sh_down, h->Fs, h->d, 256);
+  if (h->Fs && !sh8) {
+    ok &= map_bf16(&h->m_shgw, w->sh_gate, h->d, h->Fs, 256);
+    ok &= map_bf16(&h->m_shuw, w->sh_up, h->d, h->Fs, 256);
+    ok &= map_bf16(&h->m_shdw, w->sh_down, h->Fs, h->d, 256);
   }
   for (int i = 0; i < 2; ++i) {
     const int rows = 128 << i;
@@ -599,8 +613,58 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     tm.done();
     LMOE_TRY(cudaEventRecord(h->ev_latent, ss));
   }
-  // 9 shared experts gate/up + SiTU
-  if (Fs) {
+  // 9 (FP8 layers) the shared expert on the FP8 expert GEMMs: one expert that
+  // every token uses, output y_sh [T][d] fp32
+  if (Fs && h->fp8) {
+    StageTimer tm(h, LMOE_STAGE_SHARED, ss);
+    const int BNs = fp8_tile_tokens(T, 1);
+    LMOE_TRY(launch_shared_tiles(T, BNs, h->sh_tiles, h->sh_tile_off, h->sh_ntiles, ss));
+    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, ss));
+    MoeGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.a_gate = h->m_sg;
+    p.a_up = h->m_su;
+    if (!map_u8(&p.b, h->xq_sh, d, 2LL * h->Tpad_sh, 2 * BNs)) return LMOE_ERR_CUDA;
+    p.sfb = h->xsf_sh;
+    p.tiles = h->sh_tiles;
+    p.tile_off = h->sh_tile_off;
+    p.ntiles = h->sh_ntiles;
+    p.perm = h->sh_iota;
+    p.G = h->sh_ones;
+    p.err = h->err;
+    p.N_out = Fs;
+    p.MT = Fs / kFp8Rows;
+    p.KG = d / 128;
+    p.hq = h->hq_sh;
+    p.hsf = h->hsf_sh;
+    p.Fp = Fs;
+    p.act = h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0;
+    p.b1 = h->cfg.situ_beta;
+    p.b2 = h->cfg.situ_linear_beta;
+    p.wsc0 = static_cast<const float*>(h->w.sh_gate_s);
+    p.wsc1 = static_cast<const float*>(h->w.sh_up_s);
+    p.NB = Fs / 128;
+    p.KB = d / 128;
+    LMOE_TRY(launch_moe_fp8_gate_up(p, BNs, h->num_sms, ss));
+    MoeGemmParams q = p;
+    q.a_gate = h->m_sd;
+    if (!map_u8(&q.b, h->hq_sh, Fs, 2LL * h->Tpad_sh, 2 * BNs)) return LMOE_ERR_CUDA;
+    q.sfb = h->hsf_sh;
+    q.N_out = d;
+    q.MT = ceil_div(d, 2 * kFp8Rows);
+    q.KG = Fs / 128;
+    q.y = h->y_sh;
+    q.wsc0 = static_cast<const float*>(h->w.sh_down_s);
+    q.wsc1 = nullptr;
+    q.NB = d / 128;
+    q.KB = Fs / 128;
+    LMOE_TRY(launch_moe_fp8_down(q, BNs, h->num_sms, ss));
+    launches += 4;
+    tm.done();
+    LMOE_TRY(cudaEventRecord(h->ev_join, ss));
+  }
+  // 9 shared experts gate/up + SiTU (bf16 shared MLP)
+  if (Fs && !h->fp8) {
     StageTimer tm(h, LMOE_STAGE_SHARED, ss);
     DenseParams p;
     std::memset(&p, 0, sizeof(p));
@@ -618,14 +682,26 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.nkb0 = nkb_d;
     p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
     p.wide = dense_wide(BN, p.splits, p.mtiles0, p.mtiles0, nt, h->num_sms);
-    p.ldo = 2 * Fs;
-    p.out = h->part_sh;
     p.err = h->err;
-    LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, ss));
-    LMOE_TRY(launch_finalize_glu_bf16(h->part_sh, p.splits, T, Fs, 2 * Fs, h->h_s,
-                                      h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
-                                      h->cfg.situ_linear_beta, ss));
-    launches += 2;
+    if (p.wide) {
+      // gate and up tiles of the same features in one CTA: the epilogue writes h_shared
+      p.epi = 2;
+      p.out16 = h->h_s;
+      p.ldo = Fs;
+      p.act = h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0;
+      p.act_b1 = h->cfg.situ_beta;
+      p.act_b2 = h->cfg.situ_linear_beta;
+      LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, ss));
+      ++launches;
+    } else {
+      p.ldo = 2 * Fs;
+      p.out = h->part_sh;
+      LMOE_TRY(launch_dense_gemm(p, 2 * p.mtiles0, BN, ss));
+      LMOE_TRY(launch_finalize_glu_bf16(h->part_sh, p.splits, T, Fs, 2 * Fs, h->h_s,
+                                        h->cfg.act == LMOE_ACT_SWIGLU ? 1 : 0, h->cfg.situ_beta,
+                                        h->cfg.situ_linear_beta, ss));
+      launches += 2;
+    }
     tm.done();
     LMOE_TRY(cudaEventRecord(h->ev_join, ss));
   }
@@ -741,15 +817,26 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.ldo = d;
     p.out = h->part;
     p.err = h->err;
-    LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
-    LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
-    launches += 2;
+    if (p.wide) {   // one K split: the epilogue writes Delta in bf16
+      p.epi = 1;
+      p.out16 = out;
+      LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+      ++launches;
+    } else {
+      LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
+      LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
+      launches += 2;
+    }
     tm.done();
   } else {
-    // non-latent layer (Kimi K2 card): Delta = sum_i G_i E_i + h_shared W_shared_down^T
+    // non-latent layer (Kimi K2 card): Delta = sum_i G_i E_i + y_shared
     StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
     int splits = 0;
-    if (Fs) {
+    if (Fs && h->fp8) {
+      LMOE_TRY(launch_finalize_sum_bf16(h->y_sh, 1, T, d, d, out, d, h->u, d, st));
+      ++launches;
+      splits = -1;
+    } else if (Fs) {
       DenseParams p;
       std::memset(&p, 0, sizeof(p));
       p.a0 = h->m_shd;
@@ -766,12 +853,20 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
       p.ldo = d;
       p.out = h->part;
       p.err = h->err;
+      if (p.wide) {   // one K split: the epilogue adds the routed sum and writes Delta in bf16
+        p.epi = 1;
+        p.out16 = out;
+        p.add = h->u;
+        p.ld_add = d;
+      }
       LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
       ++launches;
-      splits = p.splits;
+      splits = p.wide ? -1 : p.splits;
     }
-    LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, st));
-    ++launches;
+    if (splits >= 0) {
+      LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, st));
+      ++launches;
+    }
     tm.done();
   }
   const size_t n = static_cast<size_t>(T) * h->k;
@@ -813,8 +908,13 @@ lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t
     src = h->u_hat;
     want = T * h->dx * 2;
   } else if (!std::strcmp(name, "h_shared")) {
+    if (h->fp8) return LMOE_ERR_INVALID_ARG;   // FP8 layers keep h of the shared expert as hi/lo codes
     src = h->h_s;
     want = T * h->Fs * 2;
+  } else if (!std::strcmp(name, "y_shared")) {
+    if (!h->fp8 || !h->Fs) return LMOE_ERR_INVALID_ARG;
+    src = h->y_sh;
+    want = T * h->d * 4;
   } else if (!std::strcmp(name, "counts")) {
     src = h->counts;
     want = static_cast<size_t>(h->E) * 4;

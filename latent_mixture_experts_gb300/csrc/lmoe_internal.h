@@ -24,6 +24,17 @@ struct DenseParams {
   CUtensorMap a0, a1, b0, b1;
   CUtensorMap a0w, a1w;   // the same weights with 256-row boxes (used when wide)
   int wide;               // 1: each CTA computes 256 weight rows (two accumulators), BN = 256, splits = 1
+  // Epilogue: 0 = fp32 partial sums per K split into `out` (finalized by a
+  // separate kernel); 1 = bf16 out16[t][row] (+ add[t][row] when add is set),
+  // splits = 1; 2 = gate/up pair (wide, mode 1: the CTA's two tiles are gate
+  // rows and up rows of the same 128 features), bf16 out16[t][f] =
+  // act(gate, up), splits = 1.
+  int epi;
+  void* out16;
+  const float* add;
+  int ld_add;
+  int act;
+  float act_b1, act_b2;   // SiTU caps (epilogue 2)
   float* out;
   int* err;
   int mode;
@@ -102,6 +113,7 @@ inline int fp8_tile_tokens(long long assignments, int n_experts) {
   const long long m = (assignments + n_experts - 1) / n_experts;
   return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 96;
 }
+constexpr int kFp8MaxTile = 96;
 // Token tile of the grouped MXFP4 expert GEMMs from the mean assignments per
 // expert: 16 or 32 (decode; interleaved hi/lo columns, 256-row boxes), 64 or
 // 96 (prefill; split hi/lo operands, 128-row items).
@@ -155,7 +167,7 @@ struct MoeGemmParams {
   int act;
   float b1, b2;
   // down epilogue
-  __nv_bfloat16* y;              // [T*k][dx] bf16, G-scaled expert outputs (summed in fp32 by the combine)
+  float* y;                      // [T*k][dx] fp32, G-scaled expert outputs
   // FP8 weights: fp32 scale per 128 x 128 block, [E][NB][KB]; wsc1 = up scales (gate/up pass)
   const float* wsc0;
   const float* wsc1;
@@ -166,11 +178,16 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 // FP8 E4M3 weights with 128 x 128 fp32 block scales (BN 16 or 32).
 cudaError_t launch_moe_fp8_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
 cudaError_t launch_moe_fp8_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
-cudaError_t launch_dequant_fp8_block128(const uint8_t* q, const float* s, int N, int K, void* out, cudaStream_t st);
+// The shared expert of an FP8 layer runs on the FP8 expert GEMMs as one
+// expert that every token uses: its tile list for T tokens in BN-token tiles
+// (expert 0, rows i*BN.., assignments i*BN..), tile_off = {0, ntiles*BN}.
+cudaError_t launch_shared_tiles(int T, int BN, int4* tiles, int32_t* tile_off, int32_t* ntiles, cudaStream_t s);
+// iota[i] = i and ones[i] = 1 for i < n (identity rows and unit weights of the shared expert).
+cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s);
 
 // u[t] = sum_j y[t*k + j] (slot order); u_hat = w * u / sqrt(mean(u^2) + eps) -> bf16.
-cudaError_t launch_combine_norm(const __nv_bfloat16* y, int T, int k, int l, const void* norm_w, int use_norm,
-                                float eps, float* u, void* u_hat, cudaStream_t s);
+cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
+                                float* u, void* u_hat, cudaStream_t s);
 
 // Create-time repacking of the expert weights.
 cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,

@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
             if (c_base + j < nrows) {
               const int a = __shfl_sync(0xFFFFFFFFu, a_l[j / 32], j % 32);
               const float gw = __shfl_sync(0xFFFFFFFFu, g_l[j / 32], j % 32);
-              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __float2bfloat16_rn(acc[i][j] * gw);
+              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = acc[i][j] * gw;
             }
           }
         }
@@ -336,18 +336,6 @@ cudaError_t launch_fp8(const MoeGemmParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Block-scaled FP8 [N][K] (fp32 scale per 128 x 128) -> bf16 [N][K].
-__global__ void dequant_fp8_block128_kernel(const uint8_t* __restrict__ q, const float* __restrict__ s, int N, int K,
-                                            __nv_bfloat16* __restrict__ out) {
-  const int KB = (K + 127) / 128;
-  const size_t total = static_cast<size_t>(N) * K;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int n = static_cast<int>(i / K), k = static_cast<int>(i % K);
-    out[i] = __float2bfloat16_rn(e4m3_to_f32(q[i]) * s[(n / 128) * KB + k / 128]);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_moe_fp8_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s) {
@@ -367,15 +355,6 @@ cudaError_t launch_moe_fp8_down(const MoeGemmParams& p, int BN, int grid, cudaSt
     case 96: return launch_fp8<96, false>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_dequant_fp8_block128(const uint8_t* q, const float* s, int N, int K, void* out, cudaStream_t st) {
-  const size_t total = static_cast<size_t>(N) * K;
-  size_t g = (total + 255) / 256;
-  if (g > 152 * 32) g = 152 * 32;
-  dequant_fp8_block128_kernel<<<static_cast<unsigned>(g ? g : 1), 256, 0, st>>>(q, s, N, K,
-                                                                             static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
 }
 
 }  // namespace lmoe

@@ -262,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 if (j >= nrows) break;
                 const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
                 const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
-                if (f_ok)
-                  p.y[static_cast<size_t>(a) * p.N_out + f] = __float2bfloat16_rn(__uint_as_float(rg[jj]) * gw);
+                if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __uint_as_float(rg[jj]) * gw;
               }
             }
           }
@@ -322,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
               const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
               const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
-              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __float2bfloat16_rn(y);
+              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
             }
           }
         }
@@ -445,8 +444,7 @@ __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, in
 // RMSNorm (Kimi K3 card code: routed_expert_norm between the sum and the
 // up-projection).  float4 loads; the k slot loads of an element are
 // independent so they overlap.
-__global__ void __launch_bounds__(512) combine_norm_kernel(const __nv_bfloat16* __restrict__ y, int T, int k,
-                                                           int l,
+__global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restrict__ y, int T, int k, int l,
                                                            const __nv_bfloat16* __restrict__ w, int use_norm,
                                                            float eps, float* __restrict__ u_out,
                                                            __nv_bfloat16* __restrict__ u_hat) {
@@ -456,18 +454,18 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const __nv_bfloat16* 
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int l4 = l >> 2;
-  const uint2* yt = reinterpret_cast<const uint2*>(y + static_cast<size_t>(t) * k * l);   // 4 bf16 per load
+  const float4* yt = reinterpret_cast<const float4*>(y + static_cast<size_t>(t) * k * l);
   float4* ut = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * l);
   float ss = 0.f;
   for (int i = threadIdx.x; i < l4; i += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const uint2 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
-      acc.x += __uint_as_float(v.x << 16);
-      acc.y += __uint_as_float(v.x & 0xFFFF0000u);
-      acc.z += __uint_as_float(v.y << 16);
-      acc.w += __uint_as_float(v.y & 0xFFFF0000u);
+      const float4 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
     }
     cn_u4[i] = acc;
     ut[i] = acc;
@@ -584,8 +582,8 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_norm(const __nv_bfloat16* y, int T, int k, int l, const void* norm_w, int use_norm,
-                                float eps, float* u, void* u_hat, cudaStream_t s) {
+cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
+                                float* u, void* u_hat, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(l) * sizeof(float);
   if (smem > 48 * 1024) {

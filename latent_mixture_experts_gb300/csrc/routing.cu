@@ -336,7 +336,40 @@ __global__ void __launch_bounds__(32) dispatch_scatter_kernel(const int32_t* __r
   }
 }
 
+__global__ void shared_tiles_kernel(int T, int BN, int4* __restrict__ tiles, int32_t* __restrict__ tile_off,
+                                    int32_t* __restrict__ ntiles) {
+  griddep_launch();
+  griddep_wait();
+  const int nt = (T + BN - 1) / BN;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nt; i += gridDim.x * blockDim.x)
+    tiles[i] = make_int4(0, i * BN, min(BN, T - i * BN), i * BN);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    tile_off[0] = 0;
+    tile_off[1] = nt * BN;
+    *ntiles = nt;
+  }
+}
+
+__global__ void iota_ones_kernel(int32_t* __restrict__ iota, float* __restrict__ ones, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    iota[i] = i;
+    ones[i] = 1.0f;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_shared_tiles(int T, int BN, int4* tiles, int32_t* tile_off, int32_t* ntiles, cudaStream_t s) {
+  if (T <= 0 || BN <= 0) return cudaErrorInvalidValue;
+  const int nt = (T + BN - 1) / BN;
+  return launch_pdl(shared_tiles_kernel, (nt + 255) / 256, 256, 0, s, T, BN, tiles, tile_off, ntiles);
+}
+
+cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  iota_ones_kernel<<<(n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024, 256, 0, s>>>(iota, ones, n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const float* bias, int k,
                         float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s) {

@@ -43,8 +43,8 @@ def test_k2_small_steps_and_layer(k2_small):
     assert np.array_equal(layer.lmoe_debug_tensor("perm", T).cpu().numpy(), d["perm"])
     u = layer.lmoe_debug_tensor("u", T).cpu().double().numpy()      # y_routed: no latent, no norm
     assert rel_l2_per_token(u, ref["y_routed"]).max() <= 1e-2
-    hs = layer.lmoe_debug_tensor("h_shared", T).cpu().double().numpy()
-    assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
+    ys = layer.lmoe_debug_tensor("y_shared", T).cpu().double().numpy()   # shared expert on the FP8 GEMMs
+    assert rel_l2_per_token(ys, ref["y_shared"]).max() <= 1e-2
     assert_delta_close(out.cpu().double().numpy(), ref["delta"])
 
 

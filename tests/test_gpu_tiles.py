@@ -54,15 +54,22 @@ def test_all_token_tiles(wl, Ts):
 
 
 # d = 1024, Fs = 1024 at T = 10,000 (40 tiles of 256 tokens): the shared
-# gate/up GEMM (2 x 4 paired weight tiles) and the K-concatenated output GEMM
-# (4 paired tiles) run wide, two 128-row accumulators per CTA, while the
-# router and the latent GEMM keep one tile per CTA.
-WIDE = C.Workload("k3_wide_dense", replace(C.K3_TINY, d_model=1024, d_latent=512, n_experts=32, top_k=2,
+# gate/up GEMM (8 gate/up tile pairs, SiTU in the epilogue) and the
+# K-concatenated output GEMM (4 paired tiles, bf16 in the epilogue) run wide,
+# two 128-row accumulators per CTA, while the router and the latent GEMM keep
+# one tile per CTA.
+# The routing uses the top-k of the model each layer is shaped after (K3:
+# 16, K2: 8).
+WIDE = C.Workload("k3_wide_dense", replace(C.K3_TINY, d_model=1024, d_latent=512, n_experts=64, top_k=16,
                                            d_expert_ff=256, d_shared_ff=1024), T=10000, seed=54)
+# K2-shaped: its shared expert runs on the FP8 expert GEMMs (tiles of 96
+# tokens), all tokens checked.
+WIDE_K2 = C.Workload("k2_wide_dense", replace(C.K2, d_model=1024, n_experts=48, top_k=8, d_expert_ff=384,
+                                              d_shared_ff=1024), T=10000, seed=55)
 
 
-def test_wide_dense_tiles_all_tokens():
-    wl = WIDE
+@pytest.mark.parametrize("wl", [WIDE, WIDE_K2], ids=["k3_shape", "k2_shape"])
+def test_wide_dense_tiles_all_tokens(wl):
     W, x = gpu_inputs(wl)
     layer = make_layer(wl, W, max_tokens=wl.T)
     olayer = oracle_layer(wl, W)
@@ -72,8 +79,12 @@ def test_wide_dense_tiles_all_tokens():
         layer.lmoe_sync_status()
         idx = idx.cpu().numpy()
         ref = O.forward(olayer, x_bits(x), idx=idx)
-        hs = layer.lmoe_debug_tensor("h_shared", wl.T).cpu().double().numpy()
-        assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
+        if wl.cfg.expert_wfmt == "mxfp4":
+            hs = layer.lmoe_debug_tensor("h_shared", wl.T).cpu().double().numpy()
+            assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
+        else:
+            ys = layer.lmoe_debug_tensor("y_shared", wl.T).cpu().double().numpy()
+            assert rel_l2_per_token(ys, ref["y_shared"]).max() <= 1e-2
         rel, beyond = assert_delta_close(out.cpu().double().numpy(), ref["delta"])
         print(f"{wl.name} T={wl.T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
     finally:
