@@ -15,15 +15,16 @@ namespace lmoe {
 
 namespace {
 
-// MT: 128-row weight tiles per CTA.  MT = 2 (wide, prefill-sized BN = 256):
-// one 256-row A box per stage and two accumulators filling tensor memory,
-// which halves the activation bytes each CTA moves per MAC.
+// MT: 128-row weight tiles per CTA.  MT = 2 (wide, the prefill tile BN =
+// 256): one 256-row A box per stage and two accumulators filling tensor
+// memory, which halves the activation bytes each CTA moves per MAC.
 template <int BN, int MT>
 struct DenseCfg {
   static constexpr int kA = MT * 16384;        // MT x 128 rows x 64 bf16
   static constexpr int kB = BN * 128;          // BN rows x 64 bf16
   static constexpr int kStage = kA + kB;
-  static constexpr int kStages = MT == 2 ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 5 : 6));
+  static constexpr int kStagesFit = (227 * 1024 - 2048) / (kA + BN * 128);
+  static constexpr int kStages = MT == 2 ? (kStagesFit < 6 ? kStagesFit : 6) : (BN >= 256 ? 4 : (BN >= 128 ? 5 : 6));
   static constexpr int kSmem = kStages * kStage + 1024;
   static constexpr int kTmemCols = MT * BN < 32 ? 32 : MT * BN;
   static_assert(kTmemCols <= 512, "tensor memory budget");
@@ -86,9 +87,8 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
       }
       uint8_t* st = sm + s * C::kStage;
       mbar_arrive_expect_tx(&full[s], C::kStage);
-      if (pair) {
-        tma_load_2d(st, &p.a0, &full[s], kc, m0);
-        tma_load_2d(st + 16384, &p.a1, &full[s], kc, m0);
+      if (pair) {   // gate rows then up rows of features m0.. (one 256-row box of the interleaved copy)
+        tma_load_2d(st, &p.a0w, &full[s], kc, 2 * m0);
       } else {
         tma_load_2d(st, A, &full[s], kc, m0);
       }
@@ -253,6 +253,21 @@ __global__ void finalize_glu_bf16_kernel(const float* __restrict__ part, int spl
   }
 }
 
+// Shared gate/up weights with gate and up interleaved every 128 rows:
+// row r of the copy = gate row (r/256)*128 + r%256 for r%256 < 128, else up
+// row (r/256)*128 + r%256 - 128; rows past Fs are zero.
+__global__ void interleave_gate_up_kernel(const __nv_bfloat16* __restrict__ gate, const __nv_bfloat16* __restrict__ up,
+                                          int Fs, int K, __nv_bfloat16* __restrict__ out, int rows) {
+  const size_t total = static_cast<size_t>(rows) * K;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / K), c = static_cast<int>(i % K);
+    const int w = r % 256, f = (r / 256) * 128 + (w % 128);
+    const __nv_bfloat16* src = w < 128 ? gate : up;
+    out[i] = f < Fs ? src[static_cast<size_t>(f) * K + c] : __float2bfloat16_rn(0.0f);
+  }
+}
+
 int ew_grid(size_t n) {
   size_t g = (n + 255) / 256;
   return static_cast<int>(g < 152 * 16 ? (g ? g : 1) : 152 * 16);
@@ -261,6 +276,10 @@ int ew_grid(size_t n) {
 }  // namespace
 
 cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s) {
+  // A wide launch of the M-concatenated gate/up GEMM exists only as the
+  // gate/up pair (its weights come from the interleaved copy in a0w); no
+  // 256-row maps of the separate gate and up matrices are kept.
+  if (p.wide && (BN != 256 || (p.mode == 1 && p.epi != 2))) return cudaErrorInvalidValue;
   switch (BN) {
     case 32: return launch_bn<32, 1>(p, mtiles, s);
     case 64: return launch_bn<64, 1>(p, mtiles, s);
@@ -268,6 +287,14 @@ cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStre
     case 256: return p.wide ? launch_bn<256, 2>(p, mtiles, s) : launch_bn<256, 1>(p, mtiles, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_interleave_gate_up(const void* gate, const void* up, int Fs, int K, void* out, cudaStream_t s) {
+  const int rows = 2 * ((Fs + 127) / 128) * 128;
+  interleave_gate_up_kernel<<<ew_grid(static_cast<size_t>(rows) * K), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(gate), static_cast<const __nv_bfloat16*>(up), Fs, K,
+      static_cast<__nv_bfloat16*>(out), rows);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,

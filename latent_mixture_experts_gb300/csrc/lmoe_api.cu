@@ -65,7 +65,11 @@ struct lmoe_ctx {
   uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
   // static tensor maps
   CUtensorMap m_router, m_wdown, m_wup, m_shg, m_shu, m_shd;
-  CUtensorMap m_routerw, m_wdownw, m_wupw, m_shgw, m_shuw, m_shdw;   // 256-row boxes (wide dense tiles)
+  CUtensorMap m_routerw, m_wdownw, m_wupw, m_shdw;   // 256-row boxes (wide dense tiles)
+  // bf16 shared MLP: gate and up weights interleaved every 128 rows, so one
+  // 256-row box is the gate/up tile pair of 128 features (handle-owned copy)
+  void* sh_gu_il = nullptr;
+  CUtensorMap m_shgu_il;
   CUtensorMap m_exg[2], m_exu[2], m_exd[2];   // expert codes, boxes of 128 / 256 rows
   CUtensorMap m_sg, m_su, m_sd;               // FP8 shared-expert codes, 128-row boxes
   // The latent down-projection and the shared-expert gate/up GEMM need only
@@ -108,20 +112,29 @@ int expert_bn(const lmoe_ctx* h, int T) {
   return h->fp8 ? fp8_tile_tokens(static_cast<long long>(T) * h->k, h->E) : moe_bn(T, h->k, h->E);
 }
 
-// K splits of a dense GEMM: fill about one wave of CTAs, at least two
-// 64-wide k-blocks per split.
-// A dense GEMM runs wide (two 128-row weight tiles per CTA) at the prefill
-// token tile when it needs no K split and the paired tiles still fill the SMs.
-int dense_wide(int BN, int splits, int mtiles_seg0, int mtiles_seg1, int nt, int num_sms) {
-  if (BN != 256 || splits != 1) return 0;
-  return ((mtiles_seg0 + 1) / 2 + (mtiles_seg1 + 1) / 2) * nt >= num_sms ? 1 : 0;
-}
-
-int dense_splits(int mtiles, int ntiles, int nkb, int num_sms) {
-  const int tiles = mtiles * ntiles;
+// K splits of a dense GEMM over `tiles` CTA tiles: fill about one wave of
+// CTAs, at least two 64-wide k-blocks per split.
+int dense_splits(int tiles, int nkb, int num_sms) {
   int s = num_sms / std::max(tiles, 1);
   s = std::min(s, std::max(nkb / 2, 1));
   return std::max(s, 1);
+}
+
+// Launch plan of a dense GEMM with mt0 (+ mt1, M-concatenated) 128-row
+// weight tiles and nt token tiles of BN: plain (one weight tile per CTA) or
+// wide (two per CTA: one 256-row box per stage, a third fewer bytes per
+// MAC).  Wide is taken at the prefill tile (BN = 256) when the paired tiles
+// fill the SMs without a K split; under a K split it doubled the partial
+// planes to sum and measured slower at decode.
+struct DensePlan {
+  int splits, wide;
+};
+DensePlan dense_plan(int mt0, int mt1, int nt, int nkb, int BN, int num_sms, bool allow_wide) {
+  const int tiles1 = (mt0 + mt1) * nt;
+  const int s1 = dense_splits(tiles1, nkb, num_sms);
+  const int tiles2 = ((mt0 + 1) / 2 + (mt1 + 1) / 2) * nt;
+  if (allow_wide && BN == 256 && s1 == 1 && tiles2 >= num_sms) return {1, 1};
+  return {s1, 0};
 }
 
 struct Carve {
@@ -147,15 +160,15 @@ bool map_u8(CUtensorMap* m, const void* base, int K, long long rows, int box_row
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, K, rows, K, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Largest (splits x T) a dense GEMM with `mtiles` and `nkb` needs for T <= Tm.
-long long max_split_rows(int mtiles, int nkb, int Tm, int num_sms) {
+// Largest (splits x T) a dense GEMM planned by dense_plan needs for T <= Tm.
+long long max_split_rows(int mt0, int mt1, int nkb, int Tm, int num_sms, bool allow_wide) {
   long long best = 0;
   for (int T = 1; T <= Tm;) {
     const int BN = dense_bn(T);
     const int nt = ceil_div(T, BN);
-    const int s = dense_splits(mtiles, nt, nkb, num_sms);
+    const DensePlan pl = dense_plan(mt0, mt1, nt, nkb, BN, num_sms, allow_wide);
     const int Tend = std::min(Tm, nt * BN);   // same (BN, ntiles) up to here
-    best = std::max(best, static_cast<long long>(s) * Tend);
+    best = std::max(best, static_cast<long long>(pl.splits) * Tend);
     T = Tend + 1;
   }
   return best;
@@ -227,8 +240,10 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
   p.T = T;
   p.nkb = ceil_div(h->d, 64);
   p.nkb0 = p.nkb;
-  p.splits = dense_splits(p.mtiles0, ceil_div(T, BN), p.nkb, h->num_sms);
-  p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, ceil_div(T, BN), h->num_sms);
+  // plain tiles: wide ones would split K further and top-k sums every split
+  const DensePlan pl = dense_plan(p.mtiles0, 0, ceil_div(T, BN), p.nkb, BN, h->num_sms, false);
+  p.splits = pl.splits;
+  p.wide = pl.wide;
   p.ldo = h->E;
   p.out = h->part;
   p.err = h->err;
@@ -369,17 +384,20 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   long long part_elems = 0;
   {
     const int nkb_d = ceil_div(h->d, 64);
-    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->E, 128), nkb_d, h->Tm, h->num_sms) * h->E);
-    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->din, 128), nkb_d, h->Tm, h->num_sms) * h->din);
+    part_elems =
+        std::max(part_elems, max_split_rows(ceil_div(h->E, 128), 0, nkb_d, h->Tm, h->num_sms, false) * h->E);
     if (h->Fs)
       part_elems = std::max(part_elems,
-                            max_split_rows(2 * ceil_div(h->Fs, 128), nkb_d, h->Tm, h->num_sms) * 2LL * h->Fs);
+                            max_split_rows(ceil_div(h->Fs, 128), ceil_div(h->Fs, 128), nkb_d, h->Tm, h->num_sms,
+                                           true) * 2LL * h->Fs);
     const int nkb_o = ceil_div(h->din, 64) + (h->Fs ? ceil_div(h->Fs, 64) : 0);
-    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->d, 128), nkb_o, h->Tm, h->num_sms) * h->d);
+    part_elems = std::max(part_elems, max_split_rows(ceil_div(h->d, 128), 0, nkb_o, h->Tm, h->num_sms, true) * h->d);
   }
   const long long part_sh_elems = std::max(
-      h->Fs ? max_split_rows(2 * ceil_div(h->Fs, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * 2LL * h->Fs : 0LL,
-      h->din ? max_split_rows(ceil_div(h->din, 128), ceil_div(h->d, 64), h->Tm, h->num_sms) * h->din : 0LL);
+      h->Fs ? max_split_rows(ceil_div(h->Fs, 128), ceil_div(h->Fs, 128), ceil_div(h->d, 64), h->Tm, h->num_sms, true) *
+                  2LL * h->Fs
+            : 0LL,
+      h->din ? max_split_rows(ceil_div(h->din, 128), 0, ceil_div(h->d, 64), h->Tm, h->num_sms, true) * h->din : 0LL);
   const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
   const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
@@ -418,6 +436,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->sfa_gate = c.take<uint8_t>(sfa_gu_bytes, base);
     h->sfa_up = c.take<uint8_t>(sfa_gu_bytes, base);
     h->sfa_down = c.take<uint8_t>(sfa_dn_bytes, base);
+    if (h->Fs && !sh8)
+      h->sh_gu_il = c.take<uint16_t>(2 * static_cast<size_t>(ceil_div(h->Fs, 128)) * 128 * h->d, base);
     if (sh8) {
       const size_t tiles_max = static_cast<size_t>(h->Tpad_sh / 16 + 1);
       h->sh_tiles = c.take<int4>(tiles_max, base);
@@ -471,6 +491,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
        launch_relayout_sfa(sd, h->E, h->dx, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess))
     return fail(LMOE_ERR_CUDA);
   if (sh8 && launch_iota_ones(h->sh_iota, h->sh_ones, h->Tm, stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  if (h->sh_gu_il && launch_interleave_gate_up(w->sh_gate, w->sh_up, h->Fs, h->d, h->sh_gu_il, stream) != cudaSuccess)
+    return fail(LMOE_ERR_CUDA);
   h->codes_gate = w->ex_gate_q;
   h->codes_up = w->ex_up_q;
   h->codes_down = w->ex_down_q;
@@ -508,8 +530,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     ok &= map_bf16(&h->m_wupw, w->w_up_latent, h->din, h->d, 256);
   }
   if (h->Fs && !sh8) {
-    ok &= map_bf16(&h->m_shgw, w->sh_gate, h->d, h->Fs, 256);
-    ok &= map_bf16(&h->m_shuw, w->sh_up, h->d, h->Fs, 256);
+    ok &= map_bf16(&h->m_shgu_il, h->sh_gu_il, h->d, 2 * ceil_div(h->Fs, 128) * 128, 256);
     ok &= map_bf16(&h->m_shdw, w->sh_down, h->Fs, h->d, 256);
   }
   for (int i = 0; i < 2; ++i) {
@@ -599,8 +620,9 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.T = T;
     p.nkb = nkb_d;
     p.nkb0 = nkb_d;
-    p.splits = dense_splits(p.mtiles0, nt, nkb_d, h->num_sms);
-    p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
+    const DensePlan pl = dense_plan(p.mtiles0, 0, nt, nkb_d, BN, h->num_sms, true);
+    p.splits = pl.splits;
+    p.wide = pl.wide;
     p.ldo = din;
     p.out = p.splits == 1 ? h->xc : h->part_sh;
     p.err = h->err;
@@ -670,8 +692,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     std::memset(&p, 0, sizeof(p));
     p.a0 = h->m_shg;
     p.a1 = h->m_shu;
-    p.a0w = h->m_shgw;
-    p.a1w = h->m_shuw;
+    p.a0w = h->m_shgu_il;   // wide: the gate/up tile pair as one 256-row box
     if (!map_bf16(&p.b0, x, d, T, BN)) return LMOE_ERR_CUDA;
     p.mode = 1;
     p.M0 = Fs;
@@ -680,10 +701,11 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.T = T;
     p.nkb = nkb_d;
     p.nkb0 = nkb_d;
-    p.splits = dense_splits(2 * p.mtiles0, nt, nkb_d, h->num_sms);
-    p.wide = dense_wide(BN, p.splits, p.mtiles0, p.mtiles0, nt, h->num_sms);
+    const DensePlan pl = dense_plan(p.mtiles0, p.mtiles0, nt, nkb_d, BN, h->num_sms, true);
+    p.splits = pl.splits;
+    p.wide = pl.wide;
     p.err = h->err;
-    if (p.wide) {
+    if (p.wide && p.splits == 1) {
       // gate and up tiles of the same features in one CTA: the epilogue writes h_shared
       p.epi = 2;
       p.out16 = h->h_s;
@@ -812,12 +834,13 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.M0 = d;
     p.mtiles0 = ceil_div(d, 128);
     p.T = T;
-    p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
-    p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
+    const DensePlan pl = dense_plan(p.mtiles0, 0, nt, p.nkb, BN, h->num_sms, true);
+    p.splits = pl.splits;
+    p.wide = pl.wide;
     p.ldo = d;
     p.out = h->part;
     p.err = h->err;
-    if (p.wide) {   // one K split: the epilogue writes Delta in bf16
+    if (p.splits == 1) {   // one K split: the epilogue writes Delta in bf16
       p.epi = 1;
       p.out16 = out;
       LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
@@ -836,32 +859,6 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
       LMOE_TRY(launch_finalize_sum_bf16(h->y_sh, 1, T, d, d, out, d, h->u, d, st));
       ++launches;
       splits = -1;
-    } else if (Fs) {
-      DenseParams p;
-      std::memset(&p, 0, sizeof(p));
-      p.a0 = h->m_shd;
-      p.a0w = h->m_shdw;
-      if (!map_bf16(&p.b0, h->h_s, Fs, T, BN)) return LMOE_ERR_CUDA;
-      p.mode = 0;
-      p.nkb0 = ceil_div(Fs, 64);
-      p.nkb = p.nkb0;
-      p.M0 = d;
-      p.mtiles0 = ceil_div(d, 128);
-      p.T = T;
-      p.splits = dense_splits(p.mtiles0, nt, p.nkb, h->num_sms);
-      p.wide = dense_wide(BN, p.splits, p.mtiles0, 0, nt, h->num_sms);
-      p.ldo = d;
-      p.out = h->part;
-      p.err = h->err;
-      if (p.wide) {   // one K split: the epilogue adds the routed sum and writes Delta in bf16
-        p.epi = 1;
-        p.out16 = out;
-        p.add = h->u;
-        p.ld_add = d;
-      }
-      LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
-      ++launches;
-      splits = p.wide ? -1 : p.splits;
     }
     if (splits >= 0) {
       LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, st));

@@ -27,8 +27,8 @@ struct DenseParams {
   // Epilogue: 0 = fp32 partial sums per K split into `out` (finalized by a
   // separate kernel); 1 = bf16 out16[t][row] (+ add[t][row] when add is set),
   // splits = 1; 2 = gate/up pair (wide, mode 1: the CTA's two tiles are gate
-  // rows and up rows of the same 128 features), bf16 out16[t][f] =
-  // act(gate, up), splits = 1.
+  // rows and up rows of the same 128 features, one 256-row box of the
+  // interleaved copy in a0w), bf16 out16[t][f] = act(gate, up), splits = 1.
   int epi;
   void* out16;
   const float* add;
@@ -48,6 +48,10 @@ struct DenseParams {
 // mtiles and mtiles0 count 128-row tiles (a wide launch pairs them).
 cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s);
 
+// bf16 [2*ceil(Fs/128)*128][K] copy of the shared gate [Fs][K] and up [Fs][K]
+// weights, interleaved every 128 rows (gate block, up block, ...; zero rows
+// past Fs): a 256-row box of it is the gate/up tile pair of 128 features.
+cudaError_t launch_interleave_gate_up(const void* gate, const void* up, int Fs, int K, void* out, cudaStream_t s);
 // Sum `splits` partial planes [splits][T][ld] and apply an epilogue.
 cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,
                                     cudaStream_t s);

@@ -89,3 +89,31 @@ def test_wide_dense_tiles_all_tokens(wl):
         print(f"{wl.name} T={wl.T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
     finally:
         layer.close()
+
+
+# Decode-sized batches of a d = 4096 layer: every dense GEMM splits K across
+# CTAs (up to 19 splits) and sums fp32 partials; every token is checked.
+WIDE_SPLITK = C.Workload("k3_wide_splitk", replace(C.K3_TINY, d_model=4096, d_latent=2048, n_experts=32, top_k=4,
+                                                   d_expert_ff=256, d_shared_ff=4096), T=64, seed=56)
+
+
+def test_split_k_dense_all_tokens():
+    wl = WIDE_SPLITK
+    W, x = gpu_inputs(wl)
+    layer = make_layer(wl, W, max_tokens=wl.T)
+    olayer = oracle_layer(wl, W)
+    try:
+        for T in (8, 64):
+            xt = x[:T].contiguous()
+            out, idx, _ = layer.lmoe_forward(xt, return_routing=True)
+            torch.cuda.synchronize()
+            layer.lmoe_sync_status()
+            ref = O.forward(olayer, x_bits(xt), idx=idx.cpu().numpy())
+            xc = layer.lmoe_debug_tensor("xc", T).cpu().double().numpy()
+            assert np.abs(xc - ref["xc"]).max() <= 1e-4 * (1 + np.abs(ref["xc"]).max())
+            hs = layer.lmoe_debug_tensor("h_shared", T).cpu().double().numpy()
+            assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
+            rel, beyond = assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+            print(f"{wl.name} T={T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
+    finally:
+        layer.close()
