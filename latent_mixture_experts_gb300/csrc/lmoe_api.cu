@@ -44,6 +44,7 @@ struct lmoe_ctx {
   void* pool = nullptr;
   size_t pool_bytes = 0;
   int* err = nullptr;
+  int* sched = nullptr;       // item counters: routed gate/up, routed down, shared gate/up, shared down
   float* part = nullptr;
   float* part_sh = nullptr;   // split-K partials of the GEMMs on `side` (latent down, shared gate/up)
   float* xc = nullptr;
@@ -409,6 +410,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   auto carve = [&](char* base) {
     Carve c;
     h->err = c.take<int>(4, base);
+    h->sched = c.take<int>(4, base);
     h->part = c.take<float>(static_cast<size_t>(part_elems), base);
     h->part_sh = c.take<float>(static_cast<size_t>(part_sh_elems), base);
     h->xc = c.take<float>(static_cast<size_t>(h->Tm) * h->din, base);
@@ -475,7 +477,9 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     delete h;
     return s;
   };
-  if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess ||
+      cudaMemsetAsync(h->sched, 0, 4 * sizeof(int), stream) != cudaSuccess)
+    return fail(LMOE_ERR_CUDA);
   if ((h->Fs || h->din) && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
                             cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
                             cudaEventCreateWithFlags(&h->ev_latent, cudaEventDisableTiming) != cudaSuccess ||
@@ -641,7 +645,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     StageTimer tm(h, LMOE_STAGE_SHARED, ss);
     const int BNs = fp8_tile_tokens(T, 1);
     LMOE_TRY(launch_shared_tiles(T, BNs, h->sh_tiles, h->sh_tile_off, h->sh_ntiles, ss));
-    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, ss));
+    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, h->sched + 2, ss));
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.a_gate = h->m_sg;
@@ -654,6 +658,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.perm = h->sh_iota;
     p.G = h->sh_ones;
     p.err = h->err;
+    p.sched = h->sched + 2;
     p.N_out = Fs;
     p.MT = Fs / kFp8Rows;
     p.KG = d / 128;
@@ -672,6 +677,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.a_gate = h->m_sd;
     if (!map_u8(&q.b, h->hq_sh, Fs, 2LL * h->Tpad_sh, 2 * BNs)) return LMOE_ERR_CUDA;
     q.sfb = h->hsf_sh;
+    q.sched = h->sched + 3;
     q.N_out = d;
     q.MT = ceil_div(d, 2 * kFp8Rows);
     q.KG = Fs / 128;
@@ -741,9 +747,9 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
     if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched, st));
     else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, st));
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched, st));
     ++launches;
     tm.done();
   }
@@ -765,6 +771,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.perm = h->perm;
     p.G = h->G;
     p.err = h->err;
+    p.sched = h->sched;
     p.N_out = h->F;
     p.MT = ceil_div(h->F, RB);
     p.MTa = h->MTa_gu;
@@ -790,6 +797,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.sfa_gate = h->sfa_down;
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
+    q.sched = h->sched + 1;
     q.N_out = dx;
     q.MT = ceil_div(dx, 2 * RB);
     q.MTa = h->MTa_dn;

@@ -96,10 +96,10 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
 //     2*BN*b + BN + j (lo), j = r - BN*b; hi and lo are two operands of
 //     N = BN columns, scale atoms [Ppad/BN][KG][2] (BN <= 128).
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                                int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s);
 // Same from bf16 token rows (layers whose experts take x itself).
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s);
 
 // Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
 // 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
@@ -148,6 +148,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// launch_pdl for a kernel whose CTAs form clusters of cluster_x along x.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster_x,
+                                      cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = cluster_x;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct MoeGemmParams {
   CUtensorMap a_gate, a_up, b;   // FP4 weights viewed [E*N][Kp] (boxes of moe_rows_per_item rows);
                                  // activations [2*Ppad][Kp]
@@ -160,6 +181,7 @@ struct MoeGemmParams {
   const int32_t* perm;
   const float* G;                // [T*k] routing weights (down pass)
   int* err;
+  int* sched;                    // item counter of the dynamic distribution (zeroed before the launch)
   int N_out;                     // output features per expert (F for gate/up, din for down)
   int MT;                        // work-item columns per expert tile: ceil(N_out / rows per item)
   int MTa;                       // 128-row tiles per (expert, k-group) in the scale-atom layout (even)

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
   uint8_t* sf_region = sm + C::kStages * C::kTile;
   __shared__ uint64_t full[C::kStages], empty[C::kStages], part_full[C::kRing], part_empty[C::kRing];
   __shared__ uint32_t tmem_base;
+  __shared__ ItemRing ring;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
       mbar_init(&part_full[i], 1);
       mbar_init(&part_empty[i], kFp8EpiWarps * 32);
     }
+    ring_init(ring, kFp8EpiWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -130,7 +132,12 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
       tma_prefetch_desc(&p.b);
       uint32_t it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      // the next item is claimed four k-groups before the current one's last load
+      const int claim_g = KG > 4 ? KG - 4 : 0;
+      int w = static_cast<int>(blockIdx.x) < total ? static_cast<int>(blockIdx.x) : -1;
+      for (uint32_t n = 0; ok; ++n) {
+        if (!ring_put(ring, n, w, p.err) || w < 0) break;
+        int nxt = total;
         int mt;
         const int4 tile = decode_item<BN>(p, w, mt);
         const int e = tile.x, row0 = tile.y;
@@ -139,6 +146,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
         const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
         const size_t sfb_idx = static_cast<size_t>(row0 / BN) * KG;
         for (int g = 0; g < KG; ++g, ++it) {
+          if (g == claim_g) nxt = claim_item(p.sched);
           const int s = it % C::kStages;
           if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err, kErrTimeout)) {
             ok = false;
@@ -150,6 +158,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
           tma_load_2d(st_b(s), &p.b, &full[s], g * 128, 2 * row0);
           bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, C::kSfb, &full[s]);
         }
+        w = nxt < total ? nxt : -1;
       }
     }
   } else if (warp == 1) {
@@ -157,7 +166,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
       uint32_t it = 0;
       bool ok = true;
       const uint32_t sfa = tbase + C::kSfaCol;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (uint32_t n = 0; ok; ++n) {
+        if (ring_take(ring, n, p.err) < 0) break;
         for (int g = 0; g < KG; ++g, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
@@ -210,14 +220,14 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
       }
     };
     float scl[C::kNAcc][2] = {}, nscl[C::kNAcc][2] = {};
-    if (blockIdx.x < total) item_scales(blockIdx.x, scl);
-    uint32_t it = 0;
+    uint32_t it = 0, n = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    int w = ring_take_warp(ring, 0, p.err);
+    if (w >= 0) item_scales(w, scl);
+    while (w >= 0) {
       int mt;
       const int4 tile = decode_item<BN>(p, w, mt);
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      if (w + static_cast<int>(gridDim.x) < total) item_scales(w + gridDim.x, nscl);
       float acc[C::kNAcc][C::kHalf];
 #pragma unroll
       for (int i = 0; i < C::kNAcc; ++i)
@@ -252,12 +262,11 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
         tc_fence_before();
         mbar_arrive(&part_empty[pb]);
       }
-#pragma unroll
-      for (int i = 0; i < C::kNAcc; ++i) {
-        scl[i][0] = nscl[i][0];
-        scl[i][1] = nscl[i][1];
-      }
       if (!ok) break;
+      // every load of item w has been issued by now, so its successor is
+      // published: fetch that item's block scales while w is stored
+      const int wn = ring_take_warp(ring, ++n, p.err);
+      if (wn >= 0) item_scales(wn, nscl);
       if constexpr (GU) {
         const int f = mt * C::RB + 32 * q + lane;
         const bool f_ok = f < p.N_out;
@@ -316,6 +325,12 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < C::kNAcc; ++i) {
+        scl[i][0] = nscl[i][0];
+        scl[i][1] = nscl[i][1];
+      }
+      w = wn;
     }
   }
   tc_fence_before();
@@ -326,6 +341,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
 template <int BN, bool GU>
 cudaError_t launch_fp8(const MoeGemmParams& p, int grid, cudaStream_t s) {
   using C = Fp8Cfg<BN, GU>;
+  if (!p.sched) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(moe_fp8_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;

@@ -20,6 +20,8 @@
 //     multiplies by the routing weight
 //     G_i and stores the expert output of that assignment (moe_infer's
 //     weighted sum is finished by the combine kernel in slot order).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "lmoe_internal.h"
 #include "moe_common.cuh"
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint8_t* sf_region = sm + C::kStages * C::kTile;
   __shared__ uint64_t full[C::kStages], empty[C::kStages], acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint32_t tmem_base;
+  __shared__ ItemRing ring;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -78,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiWarps * 32);
     }
+    ring_init(ring, kEpiWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -108,19 +112,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       tma_prefetch_desc(&p.b);
       uint32_t it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      // the next item is claimed four k-groups before the current one's last load
+      const int claim_g = KG > 4 ? KG - 4 : 0;
+      const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
+      // second box: the up rows of the same features, or the next RB down rows
+      const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate + C::kSfa;
+      int w = static_cast<int>(blockIdx.x) < total ? static_cast<int>(blockIdx.x) : -1;
+      for (uint32_t n = 0; ok; ++n) {
+        if (!ring_put(ring, n, w, p.err) || w < 0) break;
+        int nxt = total;
         int mt;
         const int4 tile = decode_item<BN>(p, w, mt);
         const int e = tile.x, row0 = tile.y;
-        // second box: the up rows of the same features, or the next RB down rows
         const int arow = e * p.N_out + mt * C::IR;
         const int arow1 = GU ? arow : arow + C::RB;
-        const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
-        const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate + C::kSfa;
         // atoms [E][KG][MTa][512]: the atoms of an item's tiles are adjacent
         const size_t sfa_row = static_cast<size_t>(e) * KG;
         const size_t sfb_idx = static_cast<size_t>(row0 / BN) * KG;
         for (int g = 0; g < KG; ++g, ++it) {
+          if (g == claim_g) nxt = claim_item(p.sched);
           const int s = it % C::kStages;
           if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err, kErrTimeout)) {
             ok = false;
@@ -135,13 +145,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           bulk_g2s(st_sfa(s, 1), sfa1 + sfa_off, C::kSfa, &full[s]);
           bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, C::kSfb, &full[s]);
         }
+        w = nxt < total ? nxt : -1;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0, titer = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++titer) {
+      for (uint32_t n = 0; ok; ++n, ++titer) {
+        if (ring_take(ring, n, p.err) < 0) break;
         const int b = titer % C::kAccBufs;
         const uint32_t use = titer / C::kAccBufs;
         if (use > 0 && !mbar_wait(&acc_empty[b], (use - 1) & 1, p.err, kErrTimeout)) break;
@@ -186,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     // Epilogue warps: lane quarter q of TMEM = rows 32q .. 32q+31 of each 128-row tile.
     const int q = warp & 3;
     uint32_t titer = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x, ++titer) {
+    for (uint32_t n = 0;; ++n, ++titer) {
+      const int w = ring_take_warp(ring, n, p.err);
+      if (w < 0) break;
       const int b = titer % C::kAccBufs;
       const uint32_t use = titer / C::kAccBufs;
       if (!mbar_wait(&acc_full[b], use & 1, p.err, kErrTimeout)) break;
@@ -339,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 template <int BN, bool GU>
 cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
   using C = MoeCfg<BN, GU>;
+  if (!p.sched) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
@@ -381,9 +396,14 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, int split,
-                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf) {
+                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int* __restrict__ sched) {
   griddep_launch();
   griddep_wait();
+  // item counters of the two expert GEMMs that follow on this stream
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) {
+    sched[0] = 0;
+    sched[1] = 0;
+  }
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int KG = Kp / 128;
   if (gw >= T * KG) return;
@@ -495,6 +515,79 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restri
   }
 }
 
+// Small batches: the kCombineSlices CTAs of a cluster share one token's
+// row, each summing the k slots of its slice in slot order; the RMSNorm's sum
+// of squares is added across the cluster through distributed shared memory
+// (partials of the CTAs in rank order), so a token's row is read by several
+// SMs instead of one.
+constexpr int kCombineSlices = 8;
+constexpr int kCombineClusterMaxT = 256;   // tokens up to which the cluster form is used
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_norm_cluster_kernel(
+    const float* __restrict__ y, int T, int k, int l, const __nv_bfloat16* __restrict__ w, int use_norm, float eps,
+    float* __restrict__ u_out, __nv_bfloat16* __restrict__ u_hat) {
+  namespace cg = cooperative_groups;
+  griddep_launch();
+  griddep_wait();
+  cg::cluster_group cl = cg::this_cluster();
+  extern __shared__ float4 cc_u4[];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float part_ss;
+  __shared__ float tot_ss;
+  const int t = blockIdx.y;
+  const int r = static_cast<int>(cl.block_rank());
+  const int l4 = l >> 2;
+  const int per = (l4 + kCombineSlices - 1) / kCombineSlices;
+  const int i0 = r * per;
+  const int i1 = min(l4, i0 + per);
+  const float4* yt = reinterpret_cast<const float4*>(y + static_cast<size_t>(t) * k * l);
+  float4* ut = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * l);
+  float ss = 0.f;
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const float4 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    cc_u4[i - i0] = acc;
+    ut[i] = acc;
+    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.f;
+    for (int i = 0; i < kCombineThreads / 32; ++i) v += red[i];
+    part_ss = v;
+  }
+  cl.sync();   // every CTA's partial is visible cluster-wide
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < kCombineSlices ? *cl.map_shared_rank(&part_ss, threadIdx.x) : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) tot_ss = v;
+  }
+  cl.sync();   // remote reads done before any CTA of the cluster exits; tot_ss visible
+  const float rs = use_norm ? rsqrtf(tot_ss / static_cast<float>(l) + eps) : 1.0f;
+  __nv_bfloat162* ot = reinterpret_cast<__nv_bfloat162*>(u_hat + static_cast<size_t>(t) * l);
+  const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(w);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const float4 a = cc_u4[i - i0];
+    float2 w01 = make_float2(1.f, 1.f), w23 = make_float2(1.f, 1.f);
+    if (use_norm) {
+      w01 = __bfloat1622float2(w2[2 * i]);
+      w23 = __bfloat1622float2(w2[2 * i + 1]);
+    }
+    ot[2 * i] = __floats2bfloat162_rn(w01.x * a.x * rs, w01.y * a.y * rs);
+    ot[2 * i + 1] = __floats2bfloat162_rn(w23.x * a.z * rs, w23.y * a.w * rs);
+  }
+}
+
 // Scale atoms [E][KG][MTa][512]: for expert e, k-group g (128 K values) and
 // 128-row tile t, line r0 holds for c = 0..3 the four k-block scales of row
 // 128t + 32c + r0.  Tiles of one k-group are adjacent, so a 256-row box's
@@ -554,21 +647,21 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 }
 
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                                int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
   {
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<float>, blocks, 32 * warps_per_block, 0, s, xc, T, k, din,
-                                      Kp, inv_pad, BN, split, xq, xsf);
+                                      Kp, inv_pad, BN, split, xq, xsf, sched);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
@@ -576,7 +669,7 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<__nv_bfloat16>, blocks, 32 * warps_per_block, 0, s,
                                       static_cast<const __nv_bfloat16*>(x), T, k, din, Kp, inv_pad, BN, split, xq,
-                                      xsf);
+                                      xsf, sched);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
@@ -585,6 +678,17 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
 cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
                                 float* u, void* u_hat, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (T <= kCombineClusterMaxT) {
+    const int per = (l / 4 + kCombineSlices - 1) / kCombineSlices;
+    const size_t smem = static_cast<size_t>(per) * sizeof(float4);
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
+    const cudaError_t e_ = launch_pdl_cluster(combine_norm_cluster_kernel, dim3(kCombineSlices, T), kCombineThreads,
+                                              smem, kCombineSlices, s, y, T, k, l,
+                                              static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
+                                              static_cast<__nv_bfloat16*>(u_hat));
+    if (e_ != cudaSuccess) return e_;
+    return cudaGetLastError();
+  }
   const size_t smem = static_cast<size_t>(l) * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(combine_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

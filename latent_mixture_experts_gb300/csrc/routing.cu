@@ -11,6 +11,8 @@
 // over chunks and experts, then a per-chunk stable scatter.  It also lays
 // out each expert's assignments in BN-row tiles (segments padded to a
 // multiple of BN) and writes the tile list the grouped expert GEMMs walk.
+#include <algorithm>
+
 #include "common.cuh"
 #include "lmoe_internal.h"
 
@@ -18,67 +20,127 @@ namespace lmoe {
 
 namespace {
 
-constexpr int kTopkThreads = 256;
+constexpr int kTopkMaxThreads = 1024;
+constexpr int kTopkPer = kMaxExperts / kTopkMaxThreads;   // experts per thread
+constexpr int kTopkMaxK = 32;
 
-// One block per token: all threads sum the split-K partial logits (coalesced
-// over experts) and form s and c in shared memory; warp 0 then selects the
-// k largest c one at a time, each round reducing (value, index) across the
-// warp with ties to the lower index.
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ part, int splits, int T,
-                                                            int E, const float* __restrict__ bias, int k,
-                                                            float scale, int32_t* __restrict__ idx,
-                                                            float* __restrict__ G, float* __restrict__ z_out) {
+// Strict order of the selection: larger biased score first, exact ties to
+// the lower expert index (NaN scores rank below every number).
+__device__ __forceinline__ bool topk_before(float va, int ea, float vb, int eb) {
+  return va > vb || (va == vb && ea < eb);
+}
+
+// One block per token, one thread per expert.  Each thread sums its
+// expert's split-K partial logits in split order (loads issued eight at a
+// time), forms s = sigmoid(z) and c = s + b.  The k-th largest of the
+// per-warp maxima is a lower bound of the k-th largest c (k distinct experts
+// reach it), so only experts at or above it can be selected; each such
+// candidate counts the candidates that precede it in the selection order,
+// and that count is its output position.  The selection is the one of
+// sorting all experts by (c descending, index ascending) and keeping k.
+__global__ void __launch_bounds__(kTopkMaxThreads) topk_kernel(const float* __restrict__ part, int splits, int T,
+                                                              int E, const float* __restrict__ bias, int k,
+                                                              float scale, int32_t* __restrict__ idx,
+                                                              float* __restrict__ G, float* __restrict__ z_out) {
   griddep_launch();
   griddep_wait();
+  __shared__ float wmax[32];
+  __shared__ float thr;
+  __shared__ int ncand;
+  __shared__ int sel_e[kTopkMaxK];
+  __shared__ float sel_s[kTopkMaxK];
   extern __shared__ float tk_smem[];
-  float* c = tk_smem;
-  float* sg = tk_smem + E;
-  const int t = blockIdx.x;
+  float* cand_c = tk_smem;                                   // [E]
+  float* cand_s = tk_smem + E;                               // [E]
+  int* cand_e = reinterpret_cast<int*>(tk_smem + 2 * E);     // [E]
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x;
   const size_t plane = static_cast<size_t>(T) * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float z = 0.f;
-    for (int s = 0; s < splits; ++s) z += part[s * plane + static_cast<size_t>(t) * E + e];
-    z_out[static_cast<size_t>(t) * E + e] = z;
-    const float sv = sigmoidf_(z);
-    sg[e] = sv;
-    c[e] = sv + bias[e];
+  const float* pt = part + static_cast<size_t>(t) * E;
+  if (tid == 0) ncand = 0;
+
+  float cv[kTopkPer], sv[kTopkPer];
+  float m = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kTopkPer; ++q) {
+    const int e = tid + q * nthr;
+    cv[q] = -INFINITY;
+    sv[q] = 0.f;
+    if (e < E) {
+      float z = 0.f;
+      for (int s0 = 0; s0 < splits; s0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = s0 + i < splits ? __ldg(pt + (s0 + i) * plane + e) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (s0 + i < splits) z += v[i];
+      }
+      z_out[static_cast<size_t>(t) * E + e] = z;
+      sv[q] = sigmoidf_(z);
+      const float c = sv[q] + bias[e];
+      cv[q] = c == c ? c : -INFINITY;
+    }
+    m = fmaxf(m, cv[q]);
+  }
+  m = warp_max(m);
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nthr >> 5;
+    const float mv = lane < nw ? wmax[lane] : -INFINITY;
+    float th = -INFINITY;
+    if (nw >= k) {
+      int rank = 0;
+      for (int j = 0; j < nw; ++j) {
+        const float o = __shfl_sync(0xFFFFFFFFu, mv, j);
+        rank += topk_before(o, j, mv, lane) ? 1 : 0;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < nw && rank == k - 1);
+      th = __shfl_sync(0xFFFFFFFFu, mv, __ffs(hit) - 1);
+    }
+    if (lane == 0) thr = th;
   }
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  float sel_s[32];
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int e = lane; e < E; e += 32) {
-      const float v = c[e];
-      if (v > bv) {  // e increases along the lane's scan: ties keep the lower index
-        bv = v;
-        bi = e;
-      }
-    }
+  const float th = thr;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
+  for (int q = 0; q < kTopkPer; ++q) {
+    const int e = tid + q * nthr;
+    const bool is = e < E && cv[q] >= th;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, is);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&ncand, __popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (is) {
+      const int slot = base + __popc(bal & ((1u << lane) - 1u));
+      cand_c[slot] = cv[q];
+      cand_s[slot] = sv[q];
+      cand_e[slot] = e;
     }
-    if (bi < 0 || bi >= E) bi = 0;  // only if every score were NaN
-    sel_s[j] = sg[bi];
-    if (lane == 0) {
-      idx[static_cast<size_t>(t) * k + j] = bi;
-      c[bi] = -INFINITY;
-    }
-    __syncwarp();
   }
-  if (lane == 0) {
+  __syncthreads();
+  const int n = ncand;
+  for (int i = tid; i < n; i += nthr) {
+    const float v = cand_c[i];
+    const int e = cand_e[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += topk_before(cand_c[j], cand_e[j], v, e) ? 1 : 0;
+    if (rank < k) {
+      sel_e[rank] = e;
+      sel_s[rank] = cand_s[i];
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
     float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += sel_s[j];
+    if (lane == 0)
+      for (int j = 0; j < k; ++j) sum += sel_s[j];
+    sum = __shfl_sync(0xFFFFFFFFu, sum, 0);
     const float inv = scale / sum;
-    for (int j = 0; j < k; ++j) G[static_cast<size_t>(t) * k + j] = sel_s[j] * inv;
+    if (lane < k) {
+      idx[static_cast<size_t>(t) * k + lane] = sel_e[lane];
+      G[static_cast<size_t>(t) * k + lane] = sel_s[lane] * inv;
+    }
   }
 }
 
@@ -374,9 +436,11 @@ cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s) 
 cudaError_t launch_topk(const float* logit_part, int splits, int T, int E, const float* bias, int k,
                         float routed_scale, int32_t* idx, float* G, float* z_out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const size_t smem = 2 * static_cast<size_t>(E) * sizeof(float);
+  if (E > kMaxExperts || k > kTopkMaxK || k > E) return cudaErrorInvalidValue;
+  const int threads = std::min(kTopkMaxThreads, (E + 31) / 32 * 32);
+  const size_t smem = 3 * static_cast<size_t>(E) * sizeof(float);
   {
-    const cudaError_t e_ = launch_pdl(topk_kernel, T, kTopkThreads, smem, s, logit_part,
+    const cudaError_t e_ = launch_pdl(topk_kernel, T, threads, smem, s, logit_part,
                                       splits, T, E, bias, k, routed_scale, idx, G, z_out);
     if (e_ != cudaSuccess) return e_;
   }
