@@ -45,6 +45,9 @@ struct lmoe_ctx {
   size_t pool_bytes = 0;
   int* err = nullptr;
   int* sched = nullptr;       // item counters: routed gate/up, routed down, shared gate/up, shared down
+  float* gpart = nullptr;     // K-split partial gate/up sums of small batches
+  int* gcnt = nullptr;        // their arrival counters
+  int n_gcnt = 0;
   float* part = nullptr;
   float* part_sh = nullptr;   // split-K partials of the GEMMs on `side` (latent down, shared gate/up)
   float* xc = nullptr;
@@ -111,6 +114,27 @@ int moe_bn(int T, int k, int E) { return moe_tile_tokens(static_cast<long long>(
 // Token tile of the routed expert GEMMs of this handle's weight format.
 int expert_bn(const lmoe_ctx* h, int T) {
   return h->fp8 ? fp8_tile_tokens(static_cast<long long>(T) * h->k, h->E) : moe_bn(T, h->k, h->E);
+}
+
+// K splits of the routed MXFP4 expert GEMMs (1 = none) for a batch of P
+// assignments: when the weight-row items of a pass (an upper bound of its
+// tiles times the items per tile) come to fewer than two per SM, each item's
+// K range is split (up to 4 ways, to about four items per SM) so that the
+// items keep every SM streaming to the end.
+constexpr long long kKsplitMaxP = 1024;
+int expert_ksplit(const lmoe_ctx* h, long long P, bool gate_up) {
+  if (h->fp8 || P > kKsplitMaxP) return 1;
+  const int BN = moe_tile_tokens(P, h->E);
+  if (BN != 16) return 1;   // the K-split form is built for the 16-assignment tile
+  const int RB = moe_rows_per_item(BN);
+  const long long MT = gate_up ? ceil_div(h->F, RB) : ceil_div(h->dx, 2 * RB);
+  const int KG = gate_up ? h->KG_gu : h->KG_dn;
+  const long long tiles = std::min<long long>(P, P / BN + std::min<long long>(h->E, P));
+  const long long items = tiles * MT;
+  if (items >= 2LL * h->num_sms) return 1;
+  const long long want = 4LL * h->num_sms;
+  const long long ks = std::min<long long>({(want + items - 1) / items, 4LL, KG / 2});
+  return static_cast<int>(std::max(ks, 1LL));
 }
 
 // K splits of a dense GEMM over `tiles` CTA tiles: fill about one wave of
@@ -406,6 +430,15 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512;
   const bool sh8 = h->fp8 && h->Fs;   // shared expert on the FP8 expert GEMMs
   h->Tpad_sh = sh8 ? h->Tm + kFp8MaxTile : 0;
+  // K-split scratch: partial gate/up sums, arrival counters (fewer than
+  // 4 * SMs items when split), and room for the down pass's partial planes
+  long long gpart_elems = 0, y_rows = h->Pm;
+  for (long long P = 1; P <= std::min<long long>(h->Pm, kKsplitMaxP); ++P) {
+    const int kg = expert_ksplit(h, P, true), kd = expert_ksplit(h, P, false);
+    if (kg > 1) gpart_elems = std::max(gpart_elems, 2LL * kg * P * h->F);
+    y_rows = std::max(y_rows, static_cast<long long>(kd) * P);
+  }
+  h->n_gcnt = gpart_elems ? 4 * 4 * h->num_sms : 0;
 
   auto carve = [&](char* base) {
     Carve c;
@@ -429,7 +462,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->xsf = c.take<uint8_t>(xsf_bytes, base);
     h->hq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Fp, base);
     h->hsf = c.take<uint8_t>(hsf_bytes, base);
-    h->y = c.take<float>(static_cast<size_t>(h->Pm) * h->dx, base);
+    h->y = c.take<float>(static_cast<size_t>(y_rows) * h->dx, base);
     h->u = c.take<float>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->u_hat = c.take<uint16_t>(static_cast<size_t>(h->Tm) * h->dx, base);
     h->h_s = c.take<uint16_t>(static_cast<size_t>(h->Tm) * std::max(h->Fs, 1), base);
@@ -458,6 +491,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
       h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
     }
     if (pad_dn) h->pad_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->din * (h->Fp / 2), base);
+    h->gpart = c.take<float>(static_cast<size_t>(gpart_elems), base);
+    h->gcnt = c.take<int>(static_cast<size_t>(std::max(h->n_gcnt, 1)), base);
     return c.off;
   };
   h->pool_bytes = carve(nullptr);
@@ -478,7 +513,8 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     return s;
   };
   if (cudaMemsetAsync(h->err, 0, 4 * sizeof(int), stream) != cudaSuccess ||
-      cudaMemsetAsync(h->sched, 0, 4 * sizeof(int), stream) != cudaSuccess)
+      cudaMemsetAsync(h->sched, 0, 4 * sizeof(int), stream) != cudaSuccess ||
+      cudaMemsetAsync(h->gcnt, 0, std::max(h->n_gcnt, 1) * sizeof(int), stream) != cudaSuccess)
     return fail(LMOE_ERR_CUDA);
   if ((h->Fs || h->din) && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
                             cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -645,7 +681,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     StageTimer tm(h, LMOE_STAGE_SHARED, ss);
     const int BNs = fp8_tile_tokens(T, 1);
     LMOE_TRY(launch_shared_tiles(T, BNs, h->sh_tiles, h->sh_tile_off, h->sh_ntiles, ss));
-    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, h->sched + 2, ss));
+    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, h->sched + 2, nullptr, 0, ss));
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.a_gate = h->m_sg;
@@ -659,6 +695,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.G = h->sh_ones;
     p.err = h->err;
     p.sched = h->sched + 2;
+    p.KS = 1;
     p.N_out = Fs;
     p.MT = Fs / kFp8Rows;
     p.KG = d / 128;
@@ -742,18 +779,23 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
   if (s != LMOE_OK) return s;
 
+  const int KSg = expert_ksplit(h, static_cast<long long>(T) * h->k, true);
   if (din) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_latent, 0));   // x^c from the side stream
   // 5 activations -> hi/lo E4M3 in expert-tile order
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
     if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched, st));
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched,
+                                   h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
     else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched, st));
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched,
+                                        h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
     ++launches;
     tm.done();
   }
-  // 6-7 routed experts
+  // 6-7 routed experts (small batches K split)
+  const long long P = static_cast<long long>(T) * h->k;
+  const int KSd = expert_ksplit(h, P, false);
   {
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -772,6 +814,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.G = h->G;
     p.err = h->err;
     p.sched = h->sched;
+    p.KS = expert_ksplit(h, P, true);
+    p.gpart = h->gpart;
+    p.gcnt = h->gcnt;
+    p.P = static_cast<int>(P);
     p.N_out = h->F;
     p.MT = ceil_div(h->F, RB);
     p.MTa = h->MTa_gu;
@@ -798,6 +844,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
     q.sched = h->sched + 1;
+    q.KS = KSd;
+    q.y_plane = static_cast<size_t>(P) * dx;
     q.N_out = dx;
     q.MT = ceil_div(dx, 2 * RB);
     q.MTa = h->MTa_dn;
@@ -814,8 +862,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   // 8 expert sum in slot order + latent RMSNorm
   {
     StageTimer tm(h, LMOE_STAGE_COMBINE, st);
-    LMOE_TRY(launch_combine_norm(h->y, T, h->k, dx, h->w.norm_w, din && h->cfg.use_latent_norm, h->cfg.norm_eps,
-                                 h->u, h->u_hat, st));
+    LMOE_TRY(launch_combine_norm(h->y, T, h->k, dx, KSd, static_cast<size_t>(P) * dx, h->w.norm_w,
+                                 din && h->cfg.use_latent_norm, h->cfg.norm_eps, h->u, h->u_hat, h->num_sms, st));
     ++launches;
     tm.done();
   }

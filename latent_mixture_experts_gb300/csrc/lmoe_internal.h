@@ -96,10 +96,12 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
 //     2*BN*b + BN + j (lo), j = r - BN*b; hi and lo are two operands of
 //     N = BN columns, scale atoms [Ppad/BN][KG][2] (BN <= 128).
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s);
+                                int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                cudaStream_t s);
 // Same from bf16 token rows (layers whose experts take x itself).
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s);
+                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                     cudaStream_t s);
 
 // Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
 // 256-row boxes stream FP4 codes at full HBM rate; the large token tiles of
@@ -182,6 +184,15 @@ struct MoeGemmParams {
   const float* G;                // [T*k] routing weights (down pass)
   int* err;
   int* sched;                    // item counter of the dynamic distribution (zeroed before the launch)
+  // K split of small batches: weight-row item i becomes items i*KS .. i*KS+KS-1 over consecutive
+  // k-group ranges.  Gate/up: partial sums to gpart [KS][2][P][N_out], added by the last split to
+  // arrive at a lane quarter's rows (gcnt: [item][4] counters, zeroed before the launch).  Down:
+  // split s writes its partial outputs to the y plane at y + s*y_plane.
+  int KS;
+  float* gpart;
+  int* gcnt;
+  int P;
+  size_t y_plane;
   int N_out;                     // output features per expert (F for gate/up, din for down)
   int MT;                        // work-item columns per expert tile: ceil(N_out / rows per item)
   int MTa;                       // 128-row tiles per (expert, k-group) in the scale-atom layout (even)
@@ -212,8 +223,9 @@ cudaError_t launch_shared_tiles(int T, int BN, int4* tiles, int32_t* tile_off, i
 cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s);
 
 // u[t] = sum_j y[t*k + j] (slot order); u_hat = w * u / sqrt(mean(u^2) + eps) -> bf16.
-cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
-                                float* u, void* u_hat, cudaStream_t s);
+// ks > 1: y holds ks planes (partials of a K-split down pass), plane elements apart, all added.
+cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, size_t plane, const void* norm_w,
+                                int use_norm, float eps, float* u, void* u_hat, int num_sms, cudaStream_t s);
 
 // Create-time repacking of the expert weights.
 cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,

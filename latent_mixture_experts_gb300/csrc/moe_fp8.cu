@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) moe_fp8_kernel(const __grid_co
 template <int BN, bool GU>
 cudaError_t launch_fp8(const MoeGemmParams& p, int grid, cudaStream_t s) {
   using C = Fp8Cfg<BN, GU>;
-  if (!p.sched) return cudaErrorInvalidValue;
+  if (!p.sched || p.KS != 1) return cudaErrorInvalidValue;   // no K split of FP8 items
   cudaError_t e = cudaFuncSetAttribute(moe_fp8_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;

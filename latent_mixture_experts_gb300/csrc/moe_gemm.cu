@@ -61,7 +61,109 @@ struct MoeCfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-template <int BN, bool GU>
+// Gate/up epilogue of one K split of an item (interleaved layout, small
+// batches): the warp's rows of the split's partial gate and up sums go to
+// gpart, the accumulator buffer is released, and the split that arrives last
+// at these rows (counter per item and lane quarter) adds the KS partials in
+// split order and finishes them like the unsplit epilogue: h = SiTU(g, u)
+// (or SwiGLU) as hi/lo E4M3 codes and block scales for the down pass.
+template <int BN>
+__device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t acc_base, int mt, int row0,
+                                               int nrows, int wb, int ks, int q, int lane, const int* a_r,
+                                               uint64_t* acc_empty) {
+  using C = MoeCfg<BN, true>;
+  const size_t plane = static_cast<size_t>(p.P) * p.N_out;
+  float* const gp = p.gpart + static_cast<size_t>(ks) * 2 * plane;
+#pragma unroll 1
+  for (int t = 0; t < C::kTiles; ++t) {
+    if (mt * C::RB + t * 128 >= p.Fp) break;
+    const int f = mt * C::IR + t * 128 + 32 * q + lane;
+    const bool f_ok = f < p.N_out;
+#pragma unroll 1
+    for (int j0 = 0; j0 < BN; j0 += 16) {
+      if (j0 >= nrows) break;
+      uint32_t rg[32], ru[32];
+      const uint32_t a0 = acc_base + t * C::N + 2 * j0;
+      const uint32_t a1 = a0 + C::kTiles * C::N;
+      tmem_ld16(a0, *reinterpret_cast<uint32_t(*)[16]>(&rg[0]));
+      tmem_ld16(a0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rg[16]));
+      tmem_ld16(a1, *reinterpret_cast<uint32_t(*)[16]>(&ru[0]));
+      tmem_ld16(a1 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ru[16]));
+      tmem_ld_wait();
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int j = j0 + jj;
+        if (j >= nrows) break;   // warp-uniform
+        const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
+        if (f_ok) {
+          gp[static_cast<size_t>(a) * p.N_out + f] = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
+          gp[plane + static_cast<size_t>(a) * p.N_out + f] =
+              __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(acc_empty);
+  __threadfence();
+  int* const cnt = p.gcnt + static_cast<size_t>(wb) * 4 + q;
+  int old = 0;
+  if (lane == 0) old = atomicAdd(cnt, 1);
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  if (old != p.KS - 1) return;
+  __threadfence();
+  if (lane == 0) *cnt = 0;   // counters end every forward at zero
+  uint8_t* const atom = p.hsf + ((static_cast<size_t>(row0 / BN) * (p.Fp / 128)) * C::NA) * 512;
+#pragma unroll 1
+  for (int t = 0; t < C::kTiles; ++t) {
+    if (mt * C::RB + t * 128 >= p.Fp) break;
+    const int f = mt * C::IR + t * 128 + 32 * q + lane;
+    const bool f_ok = f < p.N_out;
+    const int kblk = f >> 5;   // 32-feature block = this warp
+    const int g = kblk >> 2, kb = kblk & 3;
+#pragma unroll 1
+    for (int j0 = 0; j0 < nrows; j0 += 4) {
+      float h[4];
+      HiLo e[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        h[u] = 0.f;
+        if (j < nrows) {   // warp-uniform
+          const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
+          if (f_ok) {
+            float gv = 0.f, uv = 0.f;
+            for (int s = 0; s < p.KS; ++s) {
+              const float* src = p.gpart + static_cast<size_t>(s) * 2 * plane + static_cast<size_t>(a) * p.N_out + f;
+              gv += __ldcg(src);
+              uv += __ldcg(src + plane);
+            }
+            h[u] = glu_act_fast(gv, uv, p.act, p.b1, p.b2);
+          }
+        }
+      }
+      quant_hilo_warp_n<4>(h, e);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        if (j >= nrows) break;
+        const size_t r = static_cast<size_t>(row0) + j;
+        p.hq[(2 * r) * p.Fp + f] = e[u].q_hi;
+        p.hq[(2 * r + 1) * p.Fp + f] = e[u].q_lo;
+        if (lane == 0) {
+          const int n = 2 * j;   // MMA column of the hi term in the down pass
+          uint8_t* at = atom + static_cast<size_t>(g) * C::NA * 512;
+          at[(n >> 7) * 512 + sf_atom_offset(n & 127, kb)] = static_cast<uint8_t>(e[u].s_hi);
+          at[((n + 1) >> 7) * 512 + sf_atom_offset((n + 1) & 127, kb)] = static_cast<uint8_t>(e[u].s_lo);
+        }
+      }
+    }
+  }
+}
+
+// KSP: the K-split form for small batches (p.KS splits per item); without it
+// p.KS is taken as 1.
+template <int BN, bool GU, bool KSP>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
   using C = MoeCfg<BN, GU>;
   extern __shared__ uint8_t smem_raw[];
@@ -96,8 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const uint32_t tbase = tmem_base;
 
   const int ntiles = *p.ntiles;
-  const int total = ntiles * p.MT;
+  const int KS = KSP ? p.KS : 1;
+  const int total = ntiles * p.MT * KS;
   const int KG = p.KG;
+  // k-groups [g0, g1) of item w (the whole K range unless the batch is K split)
+  auto krange = [&](int w, int& g0, int& g1) {
+    const int ks = w % KS;
+    g0 = ks * KG / KS;
+    g1 = (ks + 1) * KG / KS;
+  };
 
   // stage sub-buffers: swizzled tiles first, all scale atoms after them
   auto st_a = [&](int s, int j) { return sm + s * C::kTile + j * C::kA; };
@@ -112,8 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       tma_prefetch_desc(&p.b);
       uint32_t it = 0;
       bool ok = true;
-      // the next item is claimed four k-groups before the current one's last load
-      const int claim_g = KG > 4 ? KG - 4 : 0;
       const CUtensorMap* map1 = GU ? &p.a_up : &p.a_gate;
       // second box: the up rows of the same features, or the next RB down rows
       const uint8_t* sfa1 = GU ? p.sfa_up : p.sfa_gate + C::kSfa;
@@ -122,14 +229,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (!ring_put(ring, n, w, p.err) || w < 0) break;
         int nxt = total;
         int mt;
-        const int4 tile = decode_item<BN>(p, w, mt);
+        const int4 tile = decode_item<BN>(p, w / KS, mt);
         const int e = tile.x, row0 = tile.y;
         const int arow = e * p.N_out + mt * C::IR;
         const int arow1 = GU ? arow : arow + C::RB;
         // atoms [E][KG][MTa][512]: the atoms of an item's tiles are adjacent
         const size_t sfa_row = static_cast<size_t>(e) * KG;
         const size_t sfb_idx = static_cast<size_t>(row0 / BN) * KG;
-        for (int g = 0; g < KG; ++g, ++it) {
+        int g0, g1;
+        krange(w, g0, g1);
+        // the next item is claimed four k-groups before this one's last load
+        const int claim_g = g1 - g0 > 4 ? g1 - 4 : g0;
+        for (int g = g0; g < g1; ++g, ++it) {
           if (g == claim_g) nxt = claim_item(p.sched);
           const int s = it % C::kStages;
           if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err, kErrTimeout)) {
@@ -153,13 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       uint32_t it = 0, titer = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n, ++titer) {
-        if (ring_take(ring, n, p.err) < 0) break;
+        const int w = ring_take(ring, n, p.err);
+        if (w < 0) break;
+        int g0, g1;
+        krange(w, g0, g1);
         const int b = titer % C::kAccBufs;
         const uint32_t use = titer / C::kAccBufs;
         if (use > 0 && !mbar_wait(&acc_empty[b], (use - 1) & 1, p.err, kErrTimeout)) break;
         tc_fence_after();
         const uint32_t d0 = tbase + b * C::kAcc;
-        for (int g = 0; g < KG; ++g, ++it) {
+        for (int g = g0; g < g1; ++g, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
             ok = false;
@@ -179,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
             const uint32_t idesc = idesc_mxf8f6f4(128, C::N, 5, 0, kb, kb);
-            const uint32_t acc = (g | kb) != 0;
+            const uint32_t acc = ((g - g0) | kb) != 0;
 #pragma unroll
             for (int i = 0; i < C::kNAcc; ++i) {
               const uint32_t a_addr = smem_u32(st_a(s, i / C::kTiles)) + (i % C::kTiles) * 16384 + 32 * kb;
@@ -205,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint32_t use = titer / C::kAccBufs;
       if (!mbar_wait(&acc_full[b], use & 1, p.err, kErrTimeout)) break;
       tc_fence_after();
+      const int wb = w / KS, ks = w - wb * KS;
       int mt;
-      const int4 tile = decode_item<BN>(p, w, mt);
+      const int4 tile = decode_item<BN>(p, wb, mt);
       const int row0 = tile.y, nrows = tile.z, p0 = tile.w;
-      // down pass: assignment and routing weight of the tile's rows j = lane + 32r
+      // assignment (and, down pass, routing weight) of the tile's rows j = lane + 32r
       constexpr int kR = (BN + 31) / 32;
       int a_r[kR];
       float g_r[kR];
@@ -216,12 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       for (int r = 0; r < kR; ++r) {
         a_r[r] = 0;
         g_r[r] = 0.f;
-        if (!GU && lane + 32 * r < nrows) {
+        if ((!GU || KSP) && lane + 32 * r < nrows) {
           a_r[r] = p.perm[p0 + lane + 32 * r];
           g_r[r] = p.G[a_r[r]];
         }
       }
       const uint32_t acc_base = tbase + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAcc;
+      // down pass: this split's output plane
+      float* const yk = KSP ? p.y + static_cast<size_t>(ks) * p.y_plane : p.y;
+      if constexpr (GU && KSP) {
+        ksplit_gate_up<BN>(p, acc_base, mt, row0, nrows, wb, ks, q, lane, a_r, &acc_empty[b]);
+        continue;
+      }
 #pragma unroll 1
       for (int t = 0; t < (GU ? C::kTiles : C::kNAcc); ++t) {
         // A 256-row item can run past the last 128-row tile of h (whose rows
@@ -276,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 if (j >= nrows) break;
                 const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
                 const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
-                if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = __uint_as_float(rg[jj]) * gw;
+                if (f_ok) yk[static_cast<size_t>(a) * p.N_out + f] = __uint_as_float(rg[jj]) * gw;
               }
             }
           }
@@ -335,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const int a = __shfl_sync(0xFFFFFFFFu, a_r[j >> 5], j & 31);
               const float gw = __shfl_sync(0xFFFFFFFFu, g_r[j >> 5], j & 31);
               const float y = (__uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1])) * gw;
-              if (f_ok) p.y[static_cast<size_t>(a) * p.N_out + f] = y;
+              if (f_ok) yk[static_cast<size_t>(a) * p.N_out + f] = y;
             }
           }
         }
@@ -350,18 +471,29 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int BN, bool GU>
-cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
+template <int BN, bool GU, bool KSP>
+cudaError_t launch_moe_k(const MoeGemmParams& p, int grid, cudaStream_t s) {
   using C = MoeCfg<BN, GU>;
-  if (!p.sched) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<BN, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<BN, GU, KSP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
   {
-    const cudaError_t e_ = launch_pdl(moe_gemm_kernel<BN, GU>, grid, kThreads, C::kSmem, s, p);
+    const cudaError_t e_ = launch_pdl(moe_gemm_kernel<BN, GU, KSP>, grid, kThreads, C::kSmem, s, p);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
+}
+
+// The K-split form exists for the 16-assignment tile, the one small batches use.
+template <int BN, bool GU>
+cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
+  if (!p.sched || p.KS < 1 || p.KS > p.KG) return cudaErrorInvalidValue;
+  if (p.KS == 1) return launch_moe_k<BN, GU, false>(p, grid, s);
+  if constexpr (BN == 16) {
+    if (GU && (!p.gpart || !p.gcnt)) return cudaErrorInvalidValue;
+    return launch_moe_k<16, GU, true>(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------ activation encode
@@ -396,13 +528,15 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
                                     const int32_t* __restrict__ inv_pad, int BN, int split,
-                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int* __restrict__ sched) {
+                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int* __restrict__ sched,
+                                    int* __restrict__ cnt, int ncnt) {
   griddep_launch();
   griddep_wait();
-  // item counters of the two expert GEMMs that follow on this stream
-  if (sched && blockIdx.x == 0 && threadIdx.x == 0) {
-    sched[0] = 0;
-    sched[1] = 0;
+  // item counters of the two expert GEMMs that follow on this stream, and
+  // the K-split arrival counters of the gate/up GEMM
+  if (blockIdx.x == 0) {
+    if (sched && threadIdx.x < 2) sched[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   }
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int KG = Kp / 128;
@@ -465,6 +599,7 @@ __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, in
 // up-projection).  float4 loads; the k slot loads of an element are
 // independent so they overlap.
 __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restrict__ y, int T, int k, int l,
+                                                           int ks, size_t plane,
                                                            const __nv_bfloat16* __restrict__ w, int use_norm,
                                                            float eps, float* __restrict__ u_out,
                                                            __nv_bfloat16* __restrict__ u_hat) {
@@ -479,13 +614,16 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restri
   float ss = 0.f;
   for (int i = threadIdx.x; i < l4; i += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < ks; ++s) {   // K-split planes of the down pass
+      const float4* ys = yt + s * (plane >> 2);
 #pragma unroll 8
-    for (int j = 0; j < k; ++j) {
-      const float4 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      for (int j = 0; j < k; ++j) {
+        const float4 v = __ldg(ys + static_cast<size_t>(j) * l4 + i);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
     }
     cn_u4[i] = acc;
     ut[i] = acc;
@@ -516,23 +654,27 @@ __global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restri
 }
 
 // Small batches: the kCombineSlices CTAs of a cluster share one token's
-// row, each summing the k slots of its slice in slot order; the RMSNorm's sum
-// of squares is added across the cluster through distributed shared memory
-// (partials of the CTAs in rank order), so a token's row is read by several
-// SMs instead of one.
+// row.  Inside a CTA, G thread groups (blockDim = 128 G; more groups the
+// fewer the tokens, so the CTAs still fill the SMs) each add every G-th of
+// the (plane, slot) terms of an element, and the group sums are added in
+// group order; the RMSNorm's sum of squares is added across
+// the cluster through distributed shared memory (partials of the CTAs in rank
+// order).  A token's row is read by several SMs with many loads in flight,
+// instead of by one block.
 constexpr int kCombineSlices = 8;
 constexpr int kCombineClusterMaxT = 256;   // tokens up to which the cluster form is used
-constexpr int kCombineThreads = 128;
+constexpr int kCombineLanes = 128;         // float4 columns of a slice handled at once
+constexpr int kCombineMaxGroups = 8;
 
-__global__ void __launch_bounds__(kCombineThreads) combine_norm_cluster_kernel(
-    const float* __restrict__ y, int T, int k, int l, const __nv_bfloat16* __restrict__ w, int use_norm, float eps,
-    float* __restrict__ u_out, __nv_bfloat16* __restrict__ u_hat) {
+__global__ void __launch_bounds__(kCombineLanes * kCombineMaxGroups) combine_norm_cluster_kernel(
+    const float* __restrict__ y, int T, int k, int l, int ks, size_t plane, const __nv_bfloat16* __restrict__ w,
+    int use_norm, float eps, float* __restrict__ u_out, __nv_bfloat16* __restrict__ u_hat) {
   namespace cg = cooperative_groups;
   griddep_launch();
   griddep_wait();
   cg::cluster_group cl = cg::this_cluster();
-  extern __shared__ float4 cc_u4[];
-  __shared__ float red[kCombineThreads / 32];
+  extern __shared__ float4 cc_part[];   // [G][per]; group 0's row then holds u
+  __shared__ float red[kCombineLanes / 32];
   __shared__ float part_ss;
   __shared__ float tot_ss;
   const int t = blockIdx.y;
@@ -541,29 +683,51 @@ __global__ void __launch_bounds__(kCombineThreads) combine_norm_cluster_kernel(
   const int per = (l4 + kCombineSlices - 1) / kCombineSlices;
   const int i0 = r * per;
   const int i1 = min(l4, i0 + per);
+  const int lane_c = threadIdx.x % kCombineLanes, grp = threadIdx.x / kCombineLanes;
+  const int groups = blockDim.x / kCombineLanes;
   const float4* yt = reinterpret_cast<const float4*>(y + static_cast<size_t>(t) * k * l);
-  float4* ut = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * l);
-  float ss = 0.f;
-  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+  const size_t plane4 = plane >> 2;
+  const int terms = ks * k;
+  for (int i = i0 + lane_c; i < i1; i += kCombineLanes) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // term q = s*k + j (plane s, slot j) for q = grp, grp + groups, ...
+    int s = grp / k, j = grp - (grp / k) * k;
 #pragma unroll 8
-    for (int j = 0; j < k; ++j) {
-      const float4 v = __ldg(yt + static_cast<size_t>(j) * l4 + i);
+    for (int q = grp; q < terms; q += groups) {
+      const float4 v = __ldg(yt + s * plane4 + static_cast<size_t>(j) * l4 + i);
+      for (j += groups; j >= k; j -= k) ++s;
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
       acc.w += v.w;
     }
-    cc_u4[i - i0] = acc;
-    ut[i] = acc;
-    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+    cc_part[grp * per + (i - i0)] = acc;
   }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float ss = 0.f;
+  if (grp == 0) {
+    float4* ut = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * l);
+    for (int i = i0 + lane_c; i < i1; i += kCombineLanes) {
+      float4 a = cc_part[i - i0];
+#pragma unroll
+      for (int g = 1; g < groups; ++g) {
+        const float4 v = cc_part[g * per + (i - i0)];
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
+      }
+      cc_part[i - i0] = a;
+      ut[i] = a;
+      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     float v = 0.f;
-    for (int i = 0; i < kCombineThreads / 32; ++i) v += red[i];
+    for (int i = 0; i < kCombineLanes / 32; ++i) v += red[i];
     part_ss = v;
   }
   cl.sync();   // every CTA's partial is visible cluster-wide
@@ -577,7 +741,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_norm_cluster_kernel(
   __nv_bfloat162* ot = reinterpret_cast<__nv_bfloat162*>(u_hat + static_cast<size_t>(t) * l);
   const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(w);
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    const float4 a = cc_u4[i - i0];
+    const float4 a = cc_part[i - i0];
     float2 w01 = make_float2(1.f, 1.f), w23 = make_float2(1.f, 1.f);
     if (use_norm) {
       w01 = __bfloat1622float2(w2[2 * i]);
@@ -647,21 +811,23 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 }
 
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s) {
+                                int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
   {
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<float>, blocks, 32 * warps_per_block, 0, s, xc, T, k, din,
-                                      Kp, inv_pad, BN, split, xq, xsf, sched);
+                                      Kp, inv_pad, BN, split, xq, xsf, sched, cnt, ncnt);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, cudaStream_t s) {
+                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                     cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
@@ -669,21 +835,24 @@ cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int K
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<__nv_bfloat16>, blocks, 32 * warps_per_block, 0, s,
                                       static_cast<const __nv_bfloat16*>(x), T, k, din, Kp, inv_pad, BN, split, xq,
-                                      xsf, sched);
+                                      xsf, sched, cnt, ncnt);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void* norm_w, int use_norm, float eps,
-                                float* u, void* u_hat, cudaStream_t s) {
+cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, size_t plane, const void* norm_w,
+                                int use_norm, float eps, float* u, void* u_hat, int num_sms, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (ks < 1 || plane % 4) return cudaErrorInvalidValue;
   if (T <= kCombineClusterMaxT) {
     const int per = (l / 4 + kCombineSlices - 1) / kCombineSlices;
-    const size_t smem = static_cast<size_t>(per) * sizeof(float4);
+    int groups = kCombineMaxGroups;   // about one wave of CTAs
+    while (groups > 1 && static_cast<long long>(T) * kCombineSlices * groups > 2LL * num_sms) groups >>= 1;
+    const size_t smem = static_cast<size_t>(groups) * per * sizeof(float4);
     if (smem > 48 * 1024) return cudaErrorInvalidValue;
-    const cudaError_t e_ = launch_pdl_cluster(combine_norm_cluster_kernel, dim3(kCombineSlices, T), kCombineThreads,
-                                              smem, kCombineSlices, s, y, T, k, l,
+    const cudaError_t e_ = launch_pdl_cluster(combine_norm_cluster_kernel, dim3(kCombineSlices, T), kCombineLanes * groups,
+                                              smem, kCombineSlices, s, y, T, k, l, ks, plane,
                                               static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
                                               static_cast<__nv_bfloat16*>(u_hat));
     if (e_ != cudaSuccess) return e_;
@@ -696,7 +865,7 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, const void*
   }
   {
     const cudaError_t e_ = launch_pdl(combine_norm_kernel, T, 512, smem, s, y,
-                                      T, k, l, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
+                                      T, k, l, ks, plane, static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,
                                       static_cast<__nv_bfloat16*>(u_hat));
     if (e_ != cudaSuccess) return e_;
   }

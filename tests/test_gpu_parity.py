@@ -224,6 +224,26 @@ def test_k3_decode_full_size(k3_decode):
     assert_delta_close(out.cpu().double().numpy()[sample], ref["delta"])
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_k3_small_batch_k_split(k3_decode, T):
+    """Kimi-K3 shapes at 1-4 tokens, where the expert GEMMs split each
+    weight-row item's K range across CTAs (gate/up partials finished by the
+    last split to arrive, down partials added by the combine): every token
+    against the oracle, and repeated forwards bit-identical (the partials are
+    added in split order whatever the arrival order)."""
+    wl, W, x, layer, olayer = k3_decode
+    xs = x[:T].contiguous()
+    out, idx, Gw = layer.lmoe_forward(xs, return_routing=True)
+    again = layer.lmoe_forward(xs)
+    torch.cuda.synchronize()
+    layer.lmoe_sync_status()
+    assert torch.equal(out, again)
+    idx = idx.cpu().numpy()
+    _check_routes(wl, layer, olayer, xs, idx, Gw.cpu().numpy())
+    ref = O.forward(olayer, x_bits(xs), idx=idx)
+    assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+
+
 def test_k3_prefill_full_size():
     """T = 8192 with the Zipf-skewed bias: every token's routing checked
     for validity, sampled tokens (one on the most loaded expert) against
