@@ -24,7 +24,10 @@ struct DenseCfg {
   static constexpr int kB = BN * 128;          // BN rows x 64 bf16
   static constexpr int kStage = kA + kB;
   static constexpr int kStagesFit = (227 * 1024 - 2048) / (kA + BN * 128);
-  static constexpr int kStages = MT == 2 ? (kStagesFit < 6 ? kStagesFit : 6) : (BN >= 256 ? 4 : (BN >= 128 ? 5 : 6));
+  // decode tiles (BN <= 64) keep a stage ring of ~100 KB so two CTAs share
+  // an SM: twice the weight bytes in flight per SM of one deeper ring
+  static constexpr int kStages = MT == 2 ? (kStagesFit < 6 ? kStagesFit : 6)
+                                         : (BN >= 256 ? 4 : (BN >= 128 ? 5 : (BN >= 64 ? 4 : 5)));
   static constexpr int kSmem = kStages * kStage + 1024;
   static constexpr int kTmemCols = MT * BN < 32 ? 32 : MT * BN;
   static_assert(kTmemCols <= 512, "tensor memory budget");

@@ -156,7 +156,8 @@ struct DensePlan {
 };
 DensePlan dense_plan(int mt0, int mt1, int nt, int nkb, int BN, int num_sms, bool allow_wide) {
   const int tiles1 = (mt0 + mt1) * nt;
-  const int s1 = dense_splits(tiles1, nkb, num_sms);
+  // decode tiles (BN <= 64) leave room for two CTAs per SM: split K for two per SM
+  const int s1 = dense_splits(tiles1, nkb, BN <= 64 ? 2 * num_sms : num_sms);
   const int tiles2 = ((mt0 + 1) / 2 + (mt1 + 1) / 2) * nt;
   if (allow_wide && BN == 256 && s1 == 1 && tiles2 >= num_sms) return {1, 1};
   return {s1, 0};
