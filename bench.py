@@ -40,12 +40,11 @@ METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
 UNIT = "tokens/s"
 # DRAM bytes (read + write) per algorithmic byte of the gate/up expert
 # kernel of each weight format, from one ncu capture of the kernel as it
-# stands on a small case of the same instantiation (profiles/
-# moe_gemm_k3_e64_t8.md: 702.7 MB for 645.2 MB; profiles/
-# moe_fp8_k2_e32_t384.md: 1166.2 MB for 998.1 MB), keyed by (weight format,
-# token tile).  An entry is removed when its kernel changes until it is
-# captured again.
-GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.089, ("fp8_block128", 96): 1.168}
+# stands on a small case of the same instantiation (K3 shapes with 64
+# experts at T = 8: 702.8 MB for 645.2 MB; K2 shapes with 32 experts at
+# T = 384: 1043.2 MB for 998.1 MB), keyed by (weight format, token tile).
+# An entry is removed when its kernel changes until it is captured again.
+GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.089, ("fp8_block128", 96): 1.045}
 
 
 def expert_tile(cfg, T: int) -> int:
