@@ -276,6 +276,20 @@ int ew_grid(size_t n) {
   return static_cast<int>(g < 152 * 16 ? (g ? g : 1) : 152 * 16);
 }
 
+// Elementwise finalizers launch early (programmatic serialization) only with
+// a small grid: an early-launched grid waits resident on the SMs until its
+// predecessor ends, and a large one holds the thread slots that the other
+// stream's kernels need (at 64 tokens the activation encoder stalled behind
+// the waiting finalizer of the side stream's shared gate/up GEMM).
+constexpr int kEarlyLaunchMaxBlocks = 256;
+template <class... KArgs, class... Args>
+cudaError_t launch_ew(void (*kernel)(KArgs...), size_t n, cudaStream_t s, Args... args) {
+  const int g = ew_grid(n);
+  if (g <= kEarlyLaunchMaxBlocks) return launch_pdl(kernel, g, 256, 0, s, args...);
+  kernel<<<g, 256, 0, s>>>(static_cast<KArgs>(args)...);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dense_gemm(const DenseParams& p, int mtiles, int BN, cudaStream_t s) {
@@ -304,8 +318,7 @@ cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M,
                                     cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * M;
   {
-    const cudaError_t e_ = launch_pdl(finalize_sum_f32_kernel, ew_grid(n), 256, 0, s, part,
-                                      splits, T, M, ld, out, ldo);
+    const cudaError_t e_ = launch_ew(finalize_sum_f32_kernel, n, s, part, splits, T, M, ld, out, ldo);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
@@ -315,8 +328,8 @@ cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M
                                      const float* add_opt, int ld_add, cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * M;
   {
-    const cudaError_t e_ = launch_pdl(finalize_sum_bf16_kernel, ew_grid(n), 256, 0, s, part,
-                                      splits, T, M, ld, static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
+    const cudaError_t e_ = launch_ew(finalize_sum_bf16_kernel, n, s, part, splits, T, M, ld,
+                                     static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
@@ -326,8 +339,8 @@ cudaError_t launch_finalize_glu_bf16(const float* part, int splits, int T, int F
                                      float b1, float b2, cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * F;
   {
-    const cudaError_t e_ = launch_pdl(finalize_glu_bf16_kernel, ew_grid(n), 256, 0, s, part,
-                                      splits, T, F, ld, static_cast<__nv_bfloat16*>(out), act, b1, b2);
+    const cudaError_t e_ = launch_ew(finalize_glu_bf16_kernel, n, s, part, splits, T, F, ld,
+                                     static_cast<__nv_bfloat16*>(out), act, b1, b2);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();

@@ -1,16 +1,22 @@
 // C ABI of the Stable LatentMoE layer: handle, workspace, launch sequence.
 //
-// lmoe_forward, all on the caller's stream, no host synchronisation:
+// lmoe_forward, no host synchronisation.  Caller's stream:
 //   1 router GEMM (bf16 tcgen05, fp32 split-K partial logits)
 //   2 top-k: sum partials, sigmoid, + bias, select, renormalise
-//   3 dispatch: counting sort into BN-row expert tiles (3 kernels)
-//   4 latent down-projection x^c = x W_down^T (+ split-K sum)
-//   5 x^c rows -> hi/lo E4M3 activations in expert-tile order
-//   6 grouped gate/up MXFP4 GEMM with SiTU epilogue -> hi/lo E4M3 h
-//   7 grouped down MXFP4 GEMM, epilogue x G_i -> per-assignment outputs
+//   3 dispatch: counting sort into BN-row expert tiles (1 or 4 kernels)
+//   5 x^c rows -> hi/lo E4M3 activations in expert-tile order (after 4)
+//   6 grouped gate/up GEMM with SiTU / SwiGLU epilogue -> hi/lo E4M3 h
+//   7 grouped down GEMM, epilogue x G_i -> per-assignment outputs
 //   8 slot-ordered sum + RMSNorm -> u_hat (bf16)
-//   9 shared gate/up GEMM (M-concatenated) + SiTU -> h_shared (bf16)
 //  10 [u_hat | h_shared] x [W_up ; W_shared_down] (K-concatenated) -> Delta
+//     (after 9); FP8 layers: Delta = sum + the shared expert's output
+// Side stream of the handle, forked at entry and joined before 5 and 10:
+//   4 latent down-projection x^c = x W_down^T (+ split-K sum)
+//   9 shared gate/up GEMM + SiTU -> h_shared (bf16); FP8 layers: the whole
+//     shared expert on the FP8 expert GEMMs
+// The grouped expert GEMMs are persistent, hand out their items through a
+// counter that step 5 zeroes, and split each item's K range for batches of
+// a few tokens.  Every kernel is launched with programmatic serialization.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -108,6 +114,8 @@ lmoe_status cuda_status(cudaError_t e) {
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kRouterMaxSplits = 16;
 
 int dense_bn(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 int moe_bn(int T, int k, int E) { return moe_tile_tokens(static_cast<long long>(T) * k, E); }
@@ -266,9 +274,11 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
   p.T = T;
   p.nkb = ceil_div(h->d, 64);
   p.nkb0 = p.nkb;
-  // plain tiles: wide ones would split K further and top-k sums every split
+  // plain tiles: wide ones would split K further and top-k sums every split;
+  // at most 16 splits, so top-k reads few partial planes (one to four tokens
+  // would otherwise split the 7168-long K ~40 ways)
   const DensePlan pl = dense_plan(p.mtiles0, 0, ceil_div(T, BN), p.nkb, BN, h->num_sms, false);
-  p.splits = pl.splits;
+  p.splits = std::min(pl.splits, kRouterMaxSplits);
   p.wide = pl.wide;
   p.ldo = h->E;
   p.out = h->part;
