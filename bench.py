@@ -36,6 +36,8 @@ from dataclasses import replace
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# Forwards of the timed region whose expert kernels carry timing events.
+PROFILE_PERIOD = 8
 METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
 UNIT = "tokens/s"
 # DRAM bytes (read + write) per algorithmic byte of the gate/up expert
@@ -250,10 +252,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    # Inside the timed region only the two expert kernels carry timing events
-    # (an event between two kernels ends their launch overlap); the per-stage
-    # breakdown comes from a separate pass after it.
+    # Inside the timed region only the two expert kernels carry timing events,
+    # and only on every PROFILE_PERIOD-th forward (an event between two
+    # kernels ends their launch overlap and costs ~10 us of a one-token
+    # forward); the per-stage breakdown comes from a separate pass after it.
     layer.lmoe_set_profiling(args.steps, stages=["expert_gate_up", "expert_down"])
+    layer.lmoe_set_profiling_period(PROFILE_PERIOD)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -276,6 +280,7 @@ def run_ours(args):
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     prof = layer.lmoe_profile_get()
     n_prof = min(args.steps, 100)
+    layer.lmoe_set_profiling_period(1)
     layer.lmoe_set_profiling(n_prof)
     for i in range(n_prof):
         layer.lmoe_forward(xs[i % 4], out=out)
@@ -358,6 +363,8 @@ def run_ours(args):
                                                              "profiles/moe_fp8_k2_e32_t384.md") +
                                         "), scaled to this launch by its algorithmic bytes"),
                      "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_avg, 5),
+                     "launches_timed": int(gu_n),
+                     "timing": f"CUDA events on the launch stream around every {PROFILE_PERIOD}th timed forward's launch",
                      "peak_source": f"{pk['src']} (MEASURED_PEAKS.json "
                                     + ("bf16_tflops x 2)" if tensor_bound else "hbm_gbs)")},
         "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),
@@ -422,6 +429,7 @@ def run_sweep(args):
         est = time.perf_counter() - t0
         steps = max(10, min(args.steps, int(0.5 / max(est, 1e-5))))
         layer.lmoe_set_profiling(steps, stages=["expert_gate_up", "expert_down"])
+        layer.lmoe_set_profiling_period(PROFILE_PERIOD)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(steps):
@@ -431,6 +439,7 @@ def run_sweep(args):
         ms = e0.elapsed_time(e1) / steps
         prof = layer.lmoe_profile_get()
         n_prof = min(steps, 50)
+        layer.lmoe_set_profiling_period(1)
         layer.lmoe_set_profiling(n_prof)
         for i in range(n_prof):
             layer.lmoe_forward(xs[i % 4], out=out)

@@ -221,6 +221,13 @@ enum {
 };
 #define LMOE_PROFILE_ALL_STAGES 0x1FFu
 LMOE_API lmoe_status lmoe_set_profiling(lmoe_handle h, int reserve_forwards, uint32_t stage_mask);
+/* Time only every `every`-th call (lmoe_forward, lmoe_route, lmoe_dispatch)
+ * while profiling is enabled, counting from the call after this one or after
+ * lmoe_set_profiling, starting with that call (default 1: every call); the
+ * calls in between run without events, so a long timed loop keeps its launch
+ * overlap while the sampled calls give the stage times.  every < 1:
+ * LMOE_ERR_INVALID_ARG. */
+LMOE_API lmoe_status lmoe_set_profiling_period(lmoe_handle h, int every);
 LMOE_API lmoe_status lmoe_profile_get(lmoe_handle h, int stage, float* total_ms, int* count);
 
 /* Number of distinct experts the last lmoe_forward's batch selected

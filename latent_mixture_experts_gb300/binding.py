@@ -22,6 +22,7 @@ LMOE_W_MXFP4, LMOE_W_FP8_BLOCK128 = 0, 1
 # Every symbol include/lmoe.h declares.
 EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lmoe_dispatch",
            "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_set_profiling",
+           "lmoe_set_profiling_period",
            "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string",
            "lmoe_dispatch_noalloc")
 NOALLOC_MAX_ASSIGNMENTS = 65536
@@ -77,6 +78,7 @@ def load_library(path: str = LIB_PATH):
             "lmoe_sync_status": (I, [P, P]),
             "lmoe_last_launch_count": (I, [P]),
             "lmoe_set_profiling": (I, [P, I, ctypes.c_uint32]),
+            "lmoe_set_profiling_period": (I, [P, I]),
             "lmoe_profile_get": (I, [P, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I)]),
             "lmoe_last_active_experts": (I, [P, P]),
             "lmoe_destroy": (I, [P]),
@@ -226,6 +228,10 @@ class LatentMoE:
             for name in stages:
                 mask |= 1 << STAGES.index(name)
         _check("lmoe_set_profiling", self._lib.lmoe_set_profiling(self._h, int(reserve_forwards), mask))
+
+    def lmoe_set_profiling_period(self, every: int):
+        """Time only every `every`-th call while profiling is on."""
+        _check("lmoe_set_profiling_period", self._lib.lmoe_set_profiling_period(self._h, int(every)))
 
     def lmoe_profile_get(self) -> dict:
         """{stage name: (summed ms, launches)} since profiling was enabled."""

@@ -94,6 +94,9 @@ struct lmoe_ctx {
   // per-stage event timing
   bool prof = false;
   uint32_t prof_mask = 0;    // stages timed while profiling
+  int prof_every = 1;        // time every prof_every-th call while profiling
+  long long prof_calls = 0;  // calls since profiling was enabled
+  bool prof_now = false;     // this call records its stage events
   std::vector<cudaEvent_t> ev_free;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_used[LMOE_NUM_STAGES];
 };
@@ -226,7 +229,7 @@ struct StageTimer {
   cudaStream_t st;
   cudaEvent_t b = nullptr;
   StageTimer(lmoe_ctx* h_, int stage_, cudaStream_t st_) : h(h_), stage(stage_), st(st_) {
-    if (h->prof && (h->prof_mask >> stage & 1u) && (b = take_event(h)) != nullptr) cudaEventRecord(b, st);
+    if (h->prof_now && (h->prof_mask >> stage & 1u) && (b = take_event(h)) != nullptr) cudaEventRecord(b, st);
   }
   void done() {
     if (!b) return;
@@ -240,6 +243,11 @@ struct StageTimer {
     b = nullptr;
   }
 };
+
+// Whether the call starting now records stage events (every prof_every-th).
+void begin_call(lmoe_ctx* h) {
+  h->prof_now = h->prof && (h->prof_calls++ % h->prof_every) == 0;
+}
 
 void release_events(lmoe_ctx* h) {
   for (auto& v : h->ev_used) {
@@ -622,6 +630,7 @@ lmoe_status lmoe_route(lmoe_handle h, const void* x, int T, int32_t* topk_idx, f
   if (T == 0) return LMOE_OK;
   if (!x || !aligned(x, 16) || !topk_idx || !topk_w) return LMOE_ERR_INVALID_ARG;
   int launches = 0;
+  begin_call(h);
   lmoe_status s = run_router(h, x, T, st, launches);
   if (s != LMOE_OK) return s;
   const size_t n = static_cast<size_t>(T) * h->k;
@@ -636,6 +645,7 @@ lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t
   if (T == 0) return LMOE_OK;
   if (!topk_idx || !counts || !offsets || !perm) return LMOE_ERR_INVALID_ARG;
   int launches = 0;
+  begin_call(h);
   return run_dispatch(h, topk_idx, T, expert_bn(h, T), counts, offsets, perm, st, launches);
 }
 
@@ -649,6 +659,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   const int BN = dense_bn(T);
   const int nt = ceil_div(T, BN);
   const int nkb_d = ceil_div(d, 64);
+  begin_call(h);
 
   // Side stream: the steps that need only x overlap the router, dispatch and
   // routed experts of the caller's stream.
@@ -1010,6 +1021,7 @@ lmoe_status lmoe_set_profiling(lmoe_handle h, int reserve_forwards, uint32_t sta
   release_events(h);
   h->prof_mask = stage_mask & LMOE_PROFILE_ALL_STAGES;
   h->prof = h->prof_mask != 0;
+  h->prof_calls = 0;
   int timed = 0;
   for (int i = 0; i < LMOE_NUM_STAGES; ++i) timed += h->prof_mask >> i & 1u;
   const size_t want = static_cast<size_t>(reserve_forwards) * 2 * timed;
@@ -1018,6 +1030,13 @@ lmoe_status lmoe_set_profiling(lmoe_handle h, int reserve_forwards, uint32_t sta
     LMOE_TRY(cudaEventCreate(&e));
     h->ev_free.push_back(e);
   }
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_set_profiling_period(lmoe_handle h, int every) {
+  if (!h || every < 1) return LMOE_ERR_INVALID_ARG;
+  h->prof_every = every;
+  h->prof_calls = 0;
   return LMOE_OK;
 }
 
