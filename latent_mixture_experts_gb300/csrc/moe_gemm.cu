@@ -845,12 +845,13 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, siz
                                 int use_norm, float eps, float* u, void* u_hat, int num_sms, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (ks < 1 || plane % 4) return cudaErrorInvalidValue;
-  if (T <= kCombineClusterMaxT) {
-    const int per = (l / 4 + kCombineSlices - 1) / kCombineSlices;
-    int groups = kCombineMaxGroups;   // about one wave of CTAs
-    while (groups > 1 && static_cast<long long>(T) * kCombineSlices * groups > 2LL * num_sms) groups >>= 1;
+  const int per = (l / 4 + kCombineSlices - 1) / kCombineSlices;
+  if (T <= kCombineClusterMaxT && static_cast<size_t>(per) * sizeof(float4) <= 48 * 1024) {
+    int groups = kCombineMaxGroups;   // about one wave of CTAs, within 48 KB of group sums
+    while (groups > 1 && (static_cast<long long>(T) * kCombineSlices * groups > 2LL * num_sms ||
+                          static_cast<size_t>(groups) * per * sizeof(float4) > 48 * 1024))
+      groups >>= 1;
     const size_t smem = static_cast<size_t>(groups) * per * sizeof(float4);
-    if (smem > 48 * 1024) return cudaErrorInvalidValue;
     const cudaError_t e_ = launch_pdl_cluster(combine_norm_cluster_kernel, dim3(kCombineSlices, T), kCombineLanes * groups,
                                               smem, kCombineSlices, s, y, T, k, l, ks, plane,
                                               static_cast<const __nv_bfloat16*>(norm_w), use_norm, eps, u,

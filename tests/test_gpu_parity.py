@@ -189,6 +189,27 @@ def test_deterministic_and_host_path(mid):
     assert torch.equal(oh, a)
 
 
+def test_stage_timing_period(mid):
+    """Stage timing records one event pair per timed call and stage: with a
+    period of 3, forwards 0, 3 and 6 of seven; outputs are unchanged by it."""
+    wl, W, x, layer, olayer = mid
+    ref = layer.lmoe_forward(x).cpu()
+    layer.lmoe_set_profiling(8, stages=["expert_gate_up", "combine_norm"])
+    layer.lmoe_set_profiling_period(3)
+    for _ in range(7):
+        out = layer.lmoe_forward(x)
+    prof = layer.lmoe_profile_get()
+    assert prof["expert_gate_up"][1] == 3 and prof["combine_norm"][1] == 3
+    assert prof["expert_down"][1] == 0
+    assert prof["expert_gate_up"][0] > 0
+    assert torch.equal(out.cpu(), ref)
+    with pytest.raises(RuntimeError):
+        layer.lmoe_set_profiling_period(0)
+    layer.lmoe_set_profiling_period(1)
+    layer.lmoe_set_profiling(0)
+    layer.lmoe_sync_status()
+
+
 def test_generator_bytes_match_cpu():
     wl = C.workload("k3_decode_t64")
     for name, e in (("ex_gate", 0), ("ex_down", 895)):
