@@ -23,7 +23,7 @@ modeling_kimi_linear.py; Kimi K2 card "Mixture of experts", "All 19 steps"):
 Everything runs in float64 on weights dequantised exactly from their stored
 formats.  numpy's matmul serves as the one library primitive.
 
-Readings of points the pages leave open (each listed in the design doc):
+Readings of points the pages leave open:
   * top-k ties go to the lower expert index; a token whose k-th and
     (k+1)-th biased scores differ by less than 1e-6 is flagged, and either
     choice there is correct;
@@ -65,17 +65,26 @@ def e8m0_value(s: np.ndarray) -> np.ndarray:
     return np.exp2(np.asarray(s).astype(np.float64) - 127.0)
 
 
+# Every value the two formats can hold, from the closed forms above: a code
+# is dequantised by looking its value up (the same numbers, without
+# re-evaluating the formula for each of a matrix's millions of codes).
+E2M1_VALUES = e2m1_value(np.arange(16))
+E8M0_VALUES = e8m0_value(np.arange(256))
+
+
 def dequant_mxfp4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """codes uint8 [N, K/2] (even K in the low nibble) and E8M0 scales
-    uint8 [N, K/32] -> float64 [N, K]."""
+    uint8 [N, K/32] -> float64 [N, K]: w = e2m1(code) * 2^(scale - 127)
+    for the 32 consecutive K values each scale covers."""
     q = np.asarray(q)
     N, Kh = q.shape
     K = 2 * Kh
-    nib = np.empty((N, K), dtype=np.uint8)
-    nib[:, 0::2] = q & 0x0F
-    nib[:, 1::2] = q >> 4
-    w = e2m1_value(nib)
-    return w * np.repeat(e8m0_value(s), 32, axis=1)[:, :K]
+    nib = np.stack([q & 0x0F, q >> 4], axis=-1).reshape(N, K)   # even K index = low nibble
+    nb = -(-K // 32)
+    w = np.zeros((N, nb * 32), dtype=np.float64)
+    w[:, :K] = E2M1_VALUES[nib]
+    w = w.reshape(N, nb, 32) * E8M0_VALUES[np.asarray(s)[:, :nb]][:, :, None]
+    return w.reshape(N, nb * 32)[:, :K]
 
 
 def e4m3_value(b: np.ndarray) -> np.ndarray:
@@ -90,12 +99,16 @@ def e4m3_value(b: np.ndarray) -> np.ndarray:
     return sign * mag
 
 
+E4M3_VALUES = e4m3_value(np.arange(256))
+
+
 def dequant_fp8_block128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """E4M3 bytes [N, K] and fp32 scales [ceil(N/128), ceil(K/128)] -> float64."""
+    """E4M3 bytes [N, K] and fp32 scales [ceil(N/128), ceil(K/128)] -> float64:
+    w = e4m3(q) * scale of the 128 x 128 block holding (n, k)."""
     q = np.asarray(q)
     N, K = q.shape
     scale = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), 128, 0), 128, 1)[:N, :K]
-    return e4m3_value(q) * scale
+    return E4M3_VALUES[q] * scale
 
 
 # ------------------------------------------------------------ activations
@@ -191,9 +204,10 @@ class Layer:
     stacked arrays, W may carry ``expert_fn(name, e) -> (q, s)`` to fetch one
     expert at a time."""
 
-    def __init__(self, cfg, W: dict):
+    def __init__(self, cfg, W: dict, cache_experts: bool = True):
         self.cfg = cfg
         self.W = W
+        self.cache_experts = cache_experts   # False: dequantise an expert afresh on every use
         self._cache = {}
 
     def dense(self, name):
@@ -203,16 +217,19 @@ class Layer:
 
     def expert(self, name, e):
         key = (name, e)
-        if key not in self._cache:
-            if "expert_fn" in self.W:
-                q, s = self.W["expert_fn"](name, e)
-            else:
-                q, s = self.W[name + "_q"][e], self.W[name + "_s"][e]
-            if self.cfg.expert_wfmt == "mxfp4":
-                self._cache[key] = dequant_mxfp4(q, s)
-            else:
-                self._cache[key] = dequant_fp8_block128(q, s)
-        return self._cache[key]
+        if key in self._cache:
+            return self._cache[key]
+        if "expert_fn" in self.W:
+            q, s = self.W["expert_fn"](name, e)
+        else:
+            q, s = self.W[name + "_q"][e], self.W[name + "_s"][e]
+        if self.cfg.expert_wfmt == "mxfp4":
+            w = dequant_mxfp4(q, s)
+        else:
+            w = dequant_fp8_block128(q, s)
+        if self.cache_experts:
+            self._cache[key] = w
+        return w
 
     def shared(self, name):
         if self.cfg.expert_wfmt == "mxfp4":
