@@ -14,12 +14,18 @@ Under torchrun (N > 1) every rank runs its own replica on its own tokens
 (the layer is per-token: no collective on the data path); value = tokens of
 all ranks / the slowest rank's time.
 
-Prints one JSON line: metric/value (device-timed tokens/s), e2e (through
-lmoe_forward_host with host buffers and the copies inside the timed
-region), roofline of the dominant kernel (the grouped MXFP4 gate/up GEMM,
-algorithmic bytes over its CUDA-event time), the whole-layer HBM roofline,
-per-stage times, clocks sampled during the timed region, and the fp64
-oracle timed on the host cores as cpu_baseline.
+Prints one JSON line: metric/value (device-timed tokens/s of the headline
+workload, Kimi-K3 shapes at T = 64), e2e (through lmoe_forward_host with
+host buffers and the copies inside the timed region), roofline of the
+dominant kernel (the grouped gate/up expert GEMM: algorithmic bytes over its
+CUDA-event time against the HBM peak, or its executed MMA FLOPs against the
+measured rate of the same MMA form above the ridge), the whole layer's
+roofline fraction (max of the HBM time and the FP4 + bf16 tensor time over
+the step time), per-stage times, the tensor-pipe peaks measured in the same
+run, clocks sampled during the timed region, the fp64 oracle timed on the
+host cores as cpu_baseline, and per_config: the same measurements for the
+token-count sweep (T = 1 .. 2048, seed 4), the Zipf-skewed prefill batch
+(T = 8192) and the Kimi-K2 block (T = 4096), each with its own clocks.
 """
 from __future__ import annotations
 
@@ -37,7 +43,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # Forwards of the timed region whose expert kernels carry timing events.
-PROFILE_PERIOD = 8
+# Coprime with the 4 rotating token batches, so the sampled forwards cycle
+# through all of them.
+PROFILE_PERIOD = 7
 METRIC = "LatentMoE layer tokens/s at T=1..8192; % of HBM or FP4-TC roofline"
 UNIT = "tokens/s"
 # DRAM bytes (read + write) per algorithmic byte of the gate/up expert
@@ -166,26 +174,30 @@ def oracle_for(wl, W_dev):
     return O, Wn
 
 
-def cpu_baseline(wl, W_dev, x_dev, ntok=2) -> dict:
-    """The fp64 oracle, as it stands, on the first `ntok` tokens of a batch
-    (its routing, 16 fresh expert dequantisations per token, dense parts)."""
+def cpu_baseline(wl, W_dev, x_dev, budget_s: float = 10.0) -> dict:
+    """The fp64 oracle, as it stands, one token at a time on the first tokens
+    of a batch (its routing, k fresh expert dequantisations, dense parts)
+    until `budget_s` of CPU time has passed."""
     import numpy as np
     import torch
     O, Wn = oracle_for(wl, W_dev)
-    xb = x_dev[:ntok].cpu().view(torch.int16).numpy().view(np.uint16)
-    layer = O.Layer(wl.cfg, Wn)
+    layer = O.Layer(wl.cfg, Wn, cache_experts=False)
     for name in ("router_w", "w_down_latent", "w_up_latent", "norm_w"):
         if name in Wn:
             layer.dense(name)        # host-side fp64 copies of the dense weights: input preparation
     for name in ("sh_gate", "sh_up", "sh_down"):
         if name in Wn:
             layer.shared(name)
+    xb = x_dev.cpu().view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
-    O.forward(layer, xb)
+    n = 0
+    while n < xb.shape[0] and (n == 0 or time.perf_counter() - t0 < budget_s):
+        O.forward(layer, xb[n:n + 1])
+        n += 1
     dt = time.perf_counter() - t0
-    return {"value": ntok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{ntok} tokens of the {wl.name} batch through the fp64 oracle (routing, "
-                      f"{ntok * wl.cfg.top_k} expert dequantisations, dense parts); numpy BLAS threads = default",
+    return {"value": n / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} tokens of the {wl.name} batch, one oracle forward each (routing, "
+                      f"{wl.cfg.top_k} expert dequantisations per token, dense parts); numpy BLAS threads = default",
             "seconds": dt}
 
 
@@ -213,7 +225,199 @@ def job_throughput(world: int, tokens_per_rank_step: int, steps: int, seconds: f
     return world * tokens_per_rank_step * steps / seconds
 
 
+def sampled_forwards(steps: int, period: int = PROFILE_PERIOD) -> list:
+    """Indices of the timed forwards whose expert kernels carry events."""
+    return list(range(0, steps, period))
+
+
+# ------------------------------------------------------------ tensor peaks
+def tensor_peaks(iters: int = 150000) -> dict:
+    """Measured tensor-pipe rates (TFLOP/s, best of three) of the MMA forms,
+    from the library's own tcgen05 loop (include/lmoe_peak.h)."""
+    from latent_mixture_experts_gb300 import binding
+    return {k: round(max(binding.tc_peak(k, iters) for _ in range(3)), 1) for k in binding.TC_KINDS}
+
+
+def rooflines(cfg, T: int, U: float, ms: float, pk: dict, tc: dict | None) -> dict:
+    """The layer's roofline time for T tokens selecting U distinct experts:
+    max(bytes / HBM, routed FLOPs / FP4 peak + dense FLOPs / bf16 peak), and
+    the measured step's fraction of it; plus the fraction of the pipe the
+    kernels actually issue on (the routed MMAs run E2M1 or E4M3 weights
+    against two E4M3 activation terms on kind::mxf8f6f4)."""
+    A = accounting(cfg)
+    bytes_ = A["dense"] + U * A["expert"] + T * A["token_io"]
+    din = A["din"]
+    f_routed = T * cfg.top_k * 6 * cfg.d_expert_ff * din
+    f_dense = T * A["flops_per_token"] - f_routed
+    t_hbm = bytes_ / (pk["hbm"] * 1e9) * 1e3
+    out = {"bytes": int(bytes_), "hbm_gbs": round(bytes_ / (ms * 1e-3) / 1e9, 1),
+           "hbm_frac": round(t_hbm / ms, 4), "tflops": round(T * A["flops_per_token"] / (ms * 1e-3) / 1e12, 1)}
+    if tc:
+        fp4 = tc["mxfp4"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
+        issued = tc["e2m1_e4m3"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
+        t_tensor = (f_routed / (fp4 * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
+        t_issued = (2 * f_routed / (issued * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
+        out.update({"tensor_floor_ms": round(t_tensor, 4), "roofline_ms": round(max(t_hbm, t_tensor), 4),
+                    "frac": round(max(t_hbm, t_tensor) / ms, 4),
+                    "bound": "hbm" if t_hbm >= t_tensor else "tensor",
+                    "issued_pipe_frac": round(t_issued / ms, 4),
+                    "routed_peak": ("mxfp4" if cfg.expert_wfmt == "mxfp4" else "e4m3_e4m3") + " (measured)"})
+    else:
+        out.update({"frac": round(t_hbm / ms, 4), "bound": "hbm"})
+    return out
+
+
+def gate_up_roofline(cfg, T: int, U: float, gu_ms: float, pk: dict, tc: dict | None) -> dict:
+    """The dominant kernel, the grouped gate/up expert GEMM: its algorithmic
+    bytes (the selected experts' gate and up weights, the hi/lo activations
+    in, the hi/lo h out) over its CUDA-event time against the HBM peak, or,
+    above the ridge, its executed MMA FLOPs (two per layer FLOP: the hi and lo
+    activation terms) against the measured peak of the form it issues."""
+    A = accounting(cfg)
+    fp4 = cfg.expert_wfmt == "mxfp4"
+    k = cfg.top_k
+    gu_bytes = U * A["gu_w"] + T * k * A["gu_per_assign"]
+    gu_flops = 2.0 * T * k * 2 * cfg.d_expert_ff * A["din"]
+    issued = (tc or {}).get("e2m1_e4m3" if fp4 else "e4m3_e4m3")
+    peak_t = issued if issued else 2.0 * pk["bf16"]
+    achieved_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
+    tensor = gu_flops / gu_bytes > 1e3 * peak_t / 2 / pk["hbm"]
+    name = ("moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)" if fp4 else
+            "moe_fp8_kernel<gate/up> (grouped E4M3 x E4M3 hi/lo, block-128 promotion, tcgen05)")
+    r = {"kernel": name, "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_ms, 5)}
+    if tensor:
+        ach = 2 * gu_flops / (gu_ms * 1e-3) / 1e12
+        r.update({"bound": "tensor", "achieved": round(ach, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
+                  "frac": round(ach / peak_t, 4), "hbm_gbs": round(achieved_gbs, 1),
+                  "flops_note": "executed MMA FLOPs (two per layer FLOP: hi and lo activation terms)",
+                  "peak_source": ("measured tcgen05 loop of the same MMA form" if issued else
+                                  "fallback: MEASURED_PEAKS.json bf16_tflops x 2")})
+    else:
+        r.update({"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                  "frac": round(achieved_gbs / pk["hbm"], 4),
+                  "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"})
+    tr = GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
+    r["traffic"] = int(tr * gu_bytes) if tr else None
+    r["traffic_source"] = ("ncu dram__bytes_read+write of this kernel on a small case of the same instantiation, "
+                           "scaled to this launch by its algorithmic bytes" if tr else
+                           "no ncu capture of this instantiation as it stands")
+    return r
+
+
+def time_forwards(layer, xs, out, steps: int, stream, world: int = 1):
+    """K forwards over the rotating batches between CUDA events on the
+    stream, the expert kernels of every PROFILE_PERIOD-th forward carrying
+    their own events; clocks sampled meanwhile.  Returns (ms, clocks,
+    profile)."""
+    import torch
+    import torch.distributed as dist
+    layer.lmoe_set_profiling(steps, stages=["expert_gate_up", "expert_down"])
+    layer.lmoe_set_profiling_period(PROFILE_PERIOD)
+    clk = ClockSampler(None)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        layer.lmoe_forward(xs[i % len(xs)], out=out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop(t_start, t_end)
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    prof = layer.lmoe_profile_get()
+    layer.lmoe_set_profiling_period(1)
+    layer.lmoe_set_profiling(0)
+    return ms, clocks, prof
+
+
+def stage_pass(layer, xs, out, n: int) -> dict:
+    """Per-stage averages from a separate pass with every stage timed."""
+    layer.lmoe_set_profiling_period(1)
+    layer.lmoe_set_profiling(n)
+    for i in range(n):
+        layer.lmoe_forward(xs[i % len(xs)], out=out)
+    sp = layer.lmoe_profile_get()
+    layer.lmoe_set_profiling(0)
+    return {name: round(v[0] / max(v[1], 1), 5) for name, v in sp.items()}
+
+
+def active_experts(layer, xs, out) -> list:
+    U = []
+    for xb in xs:
+        layer.lmoe_forward(xb, out=out)
+        U.append(layer.lmoe_last_active_experts())
+    return U
+
+
+def measure_config(wl, layer, xs, out, steps_min: int, warmup: int, pk: dict, tc: dict | None,
+                   target_s: float = 0.3, max_steps: int = 4000) -> dict:
+    """One entry of the per-configuration block: tokens/s over a timed region
+    of about target_s (at least steps_min forwards), the layer's roofline
+    fraction, the dominant kernel's roofline, clocks."""
+    import torch
+    cfg, T = wl.cfg, xs[0].shape[0]
+    U = active_experts(layer, xs, out)
+    for i in range(warmup):
+        layer.lmoe_forward(xs[i % len(xs)], out=out)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(3):
+        layer.lmoe_forward(xs[i % len(xs)], out=out)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / 3
+    steps = int(min(max_steps, max(steps_min, target_s / max(est, 1e-6))))
+    stream = torch.cuda.current_stream()
+    ms, clocks, prof = time_forwards(layer, xs, out, steps, stream)
+    ms_step = ms / steps
+    samp = sampled_forwards(steps)
+    U_s = sum(U[i % len(xs)] for i in samp) / len(samp)
+    U_all = sum(U[i % len(xs)] for i in range(steps)) / steps
+    gu_ms, gu_n = prof["expert_gate_up"]
+    return {"workload": wl.name, "T": T, "steps": steps, "tokens_per_s": round(T / (ms_step * 1e-3), 1),
+            "ms_per_step": round(ms_step, 5), "active_experts_mean": round(U_all, 1),
+            "layer_roofline": rooflines(cfg, T, U_all, ms_step, pk, tc),
+            "roofline": {**gate_up_roofline(cfg, T, U_s, gu_ms / max(gu_n, 1), pk, tc), "launches_timed": int(gu_n)},
+            "clocks": clocks}
+
+
 # ------------------------------------------------------------------ ours
+# Configurations measured beside the headline one, one GPU: the token-count
+# sweep (seed 4), the Zipf-skewed prefill batch and the Kimi-K2 block.
+PER_CONFIG = (("k3_sweep", (1, 8, 32, 128, 512, 2048)), ("k3_prefill_t8192", None), ("k2_t4096", None))
+
+
+def run_per_config(args, pk, tc, budget_s: float = 240.0) -> list:
+    import torch
+    from lmoe_inputs import configs as C
+    from lmoe_inputs import generate as G
+    from latent_mixture_experts_gb300 import LatentMoE
+    entries = []
+    t_start = time.time()
+    for name, Ts in PER_CONFIG:
+        if time.time() - t_start > budget_s:
+            entries.append({"workload": name, "skipped": "time budget of the per-configuration block spent"})
+            continue
+        wl = C.workload(f"k3_sweep_t{max(Ts)}" if Ts else name)
+        W = G.gen_weights(wl, device="cuda")
+        layer = LatentMoE(wl.cfg, W, max_tokens=wl.T)
+        try:
+            for T in (Ts or (wl.T,)):
+                wlT = replace(wl, T=T, name=f"k3_sweep_t{T}") if Ts else wl
+                xs = [G.gen_x(replace(wlT, seed=sd), device="cuda") for sd in replica_seeds(wlT, 0)]
+                out = torch.empty(T, wl.cfg.d_model, dtype=torch.bfloat16, device="cuda")
+                entries.append(measure_config(wlT, layer, xs, out, args.steps, args.warmup, pk, tc))
+            layer.lmoe_sync_status()
+        finally:
+            layer.close()
+            del W
+            torch.cuda.empty_cache()
+    return entries
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -231,6 +435,8 @@ def run_ours(args):
         build.build()
     if world > 1:
         dist.barrier()
+    pk = peaks()
+    tc = None if args.no_tc_peaks else tensor_peaks()
     wl = C.workload(args.workload)
     T, cfg = wl.T, wl.cfg
     W = G.gen_weights(wl, device="cuda")
@@ -240,10 +446,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     # distinct experts each batch selects (units of the expert bytes)
-    U = []
-    for xb in xs:
-        layer.lmoe_forward(xb, out=out)
-        U.append(layer.lmoe_last_active_experts())
+    U = active_experts(layer, xs, out)
     layer.lmoe_sync_status()
     launches = layer.lmoe_last_launch_count()
 
@@ -256,66 +459,26 @@ def run_ours(args):
     # and only on every PROFILE_PERIOD-th forward (an event between two
     # kernels ends their launch overlap and costs ~10 us of a one-token
     # forward); the per-stage breakdown comes from a separate pass after it.
-    layer.lmoe_set_profiling(args.steps, stages=["expert_gate_up", "expert_down"])
-    layer.lmoe_set_profiling_period(PROFILE_PERIOD)
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
-    except Exception:
-        pass
-    clk = ClockSampler(uuid)
-    time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t_start = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        layer.lmoe_forward(xs[i % 4], out=out)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_end = time.time()
-    if world > 1:
-        dist.barrier()
-    clocks = clk.stop(t_start, t_end)
-    ms = max_over_ranks(e0.elapsed_time(e1), world)
-    prof = layer.lmoe_profile_get()
-    n_prof = min(args.steps, 100)
-    layer.lmoe_set_profiling_period(1)
-    layer.lmoe_set_profiling(n_prof)
-    for i in range(n_prof):
-        layer.lmoe_forward(xs[i % 4], out=out)
-    stage_prof = layer.lmoe_profile_get()
-    layer.lmoe_set_profiling(0)
+    ms, clocks, prof = time_forwards(layer, xs, out, args.steps, stream, world)
+    stages = stage_pass(layer, xs, out, min(args.steps, 100))
     layer.lmoe_sync_status()
 
     steps = args.steps
     ms_step = ms / steps
     value = job_throughput(world, T, steps, ms / 1e3)
     U_mean = sum(U[i % 4] for i in range(steps)) / steps
-    pk = peaks()
-
-    # dominant kernel: the grouped gate/up expert GEMM.  Algorithmic bytes
-    # per launch: the selected experts' gate+up weights (codes and scales),
-    # the hi/lo E4M3 activations in (with their scales) and the hi/lo h out.
-    A = accounting(cfg)
-    din, F, k = A["din"], cfg.d_expert_ff, cfg.top_k
-    gu_bytes = U_mean * A["gu_w"] + T * k * A["gu_per_assign"]
+    samp = sampled_forwards(steps)
+    U_samp = sum(U[i % 4] for i in samp) / len(samp)      # batches whose kernel times were taken
     gu_ms, gu_n = prof["expert_gate_up"]
-    gu_avg = gu_ms / max(gu_n, 1)
-    achieved = gu_bytes / (gu_avg * 1e-3) / 1e9
-    # The kernel's bound: HBM below the ridge of the measured peaks, the
-    # tensor pipe above it.  Its MMAs run in FP8 (E2M1 or E4M3 weights x E4M3
-    # activations) with two activation terms, i.e. two FP8 MACs per MAC of the
-    # layer; the FP8 peak is the measured bf16 peak x 2 (the nominal ratio).
-    gu_flops = 2.0 * T * k * 2 * cfg.d_expert_ff * din            # layer FLOPs of the gate/up GEMMs
-    fp8_peak = 2.0 * pk["bf16"]
-    tensor_bound = gu_flops / gu_bytes > 1e3 * pk["bf16"] / pk["hbm"]
-    dn_bytes = U_mean * A["dn_w"] + T * k * A["dn_per_assign"]
     dn_ms, dn_n = prof["expert_down"]
-    layer_bytes = A["dense"] + U_mean * A["expert"] + T * A["token_io"]
+    A = accounting(cfg)
+    dn_bytes = U_samp * A["dn_w"] + T * cfg.top_k * A["dn_per_assign"]
     fp4 = cfg.expert_wfmt == "mxfp4"
-    gu_traffic = GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
-    stages = {name: round(v[0] / max(v[1], 1), 5) for name, v in stage_prof.items()}
+    roof = gate_up_roofline(cfg, T, U_samp, gu_ms / max(gu_n, 1), pk, tc)
+    roof.update({"launches_timed": int(gu_n), "sampled_batches": sorted({i % 4 for i in samp}),
+                 "timing": f"CUDA events on the launch stream around every {PROFILE_PERIOD}th timed forward's "
+                           f"launch (forwards {samp[:6]}{'...' if len(samp) > 6 else ''}); bytes from the "
+                           "distinct experts of the batches those forwards ran"})
 
     # end to end through the host-buffer entry point
     xh = [xb.cpu().pin_memory() for xb in xs]
@@ -332,7 +495,13 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, W, xs[0], ntok=args.cpu_tokens)
+        cpu = cpu_baseline(wl, W, xs[0])
+    layer.close()
+    del W
+    torch.cuda.empty_cache()
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        per_config = run_per_config(args, pk, tc)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -343,127 +512,29 @@ def run_ours(args):
         "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to "
                 + ("MXFP4" if fp4 else "FP8 E4M3 block-128") + "; x ~ N(0,1) bf16)",
         "config": {"workload": wl.name, "T": T, "d_model": cfg.d_model, "d_latent": cfg.d_latent, "n_experts": cfg.n_experts,
-                   "top_k": k, "d_expert_ff": F, "d_shared_ff": cfg.d_shared_ff, "expert_format": cfg.expert_wfmt,
+                   "top_k": cfg.top_k, "d_expert_ff": cfg.d_expert_ff, "d_shared_ff": cfg.d_shared_ff,
+                   "expert_format": cfg.expert_wfmt,
                    "parallelism": f"replicas x{world}", "token_batches_rotated": 4,
                    "l2": "no flush: each step streams the selected experts' weights (GBs) >> 129 MB L2",
                    "active_experts_mean": round(U_mean, 1)},
-        "roofline": {"kernel": ("moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)" if fp4 else
-                                "moe_fp8_kernel<gate/up> (grouped E4M3 x E4M3 hi/lo, block-128 promotion, tcgen05)"),
-                     **({"bound": "tensor", "achieved": round(2 * gu_flops / (gu_avg * 1e-3) / 1e12, 1),
-                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                         "frac": round(2 * gu_flops / (gu_avg * 1e-3) / 1e12 / fp8_peak, 4),
-                         "flops_note": "executed FP8 FLOPs (2 per layer FLOP: hi and lo activation terms) over "
-                                       "the FP8 peak = measured bf16 peak x 2",
-                         "hbm_gbs": round(achieved, 1)} if tensor_bound else
-                        {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm"], 4)}),
-                     "traffic": int(gu_traffic * gu_bytes) if gu_traffic else None,
-                     "traffic_source": ("ncu dram__bytes_read+write of this kernel on a small case of the same "
-                                        "instantiation (" + ("profiles/moe_gemm_k3_e64_t8.md" if fp4 else
-                                                             "profiles/moe_fp8_k2_e32_t384.md") +
-                                        "), scaled to this launch by its algorithmic bytes"),
-                     "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_avg, 5),
-                     "launches_timed": int(gu_n),
-                     "timing": f"CUDA events on the launch stream around every {PROFILE_PERIOD}th timed forward's launch",
-                     "peak_source": f"{pk['src']} (MEASURED_PEAKS.json "
-                                    + ("bf16_tflops x 2)" if tensor_bound else "hbm_gbs)")},
-        "layer_roofline": {"bound": "hbm", "bytes_per_step": int(layer_bytes),
-                           "achieved": round(layer_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": pk["hbm"],
-                           "unit": "GB/s", "frac": round(layer_bytes / (ms_step * 1e-3) / 1e9 / pk["hbm"], 4),
-                           "tflops": round(T * A["flops_per_token"] / (ms_step * 1e-3) / 1e12, 1),
-                           "frac_of_bf16_peak": round(T * A["flops_per_token"] / (ms_step * 1e-3) / 1e12
-                                                      / pk["bf16"], 4),
-                           "frac_of_bf16_sustained": round(T * A["flops_per_token"] / (ms_step * 1e-3) / 1e12
-                                                           / pk["bf16_sus"], 4)},
+        "roofline": roof,
+        "layer_roofline": rooflines(cfg, T, U_mean, ms_step, pk, tc),
         "down_kernel": {"achieved": round(dn_bytes / (dn_ms / max(dn_n, 1) * 1e-3) / 1e9, 1), "unit": "GB/s",
                         "ms_per_launch": round(dn_ms / max(dn_n, 1), 5)},
         "stage_ms": stages,
-        "stage_ms_source": f"separate pass of {n_prof} forwards with every stage timed (outside the timed region)",
+        "stage_ms_source": f"separate pass of {min(steps, 100)} forwards with every stage timed (outside the timed region)",
+        "tensor_peaks_tflops": tc,
+        "tensor_peaks_source": "measured in this run: tcgen05 loop, one CTA per SM, M=128 N=256, best of 3",
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches * steps,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
     if world > 1:
         dist.destroy_process_group()
-
-
-# ------------------------------------------------------------------ sweep
-def run_sweep(args):
-    """Token-count sweep on one GPU: the K3 layer of the sweep workload (seed 4,
-    uniform bias) built once, one JSON line per T with tokens/s, the layer's
-    HBM-roofline fraction, its FLOP rate against the bf16 tensor peak (the hi/lo
-    E4M3 activations make the routed MMAs cost what bf16 would), the expert
-    kernels' GB/s and the per-stage times."""
-    import torch
-    from lmoe_inputs import configs as C
-    from lmoe_inputs import generate as G
-    from latent_mixture_experts_gb300 import LatentMoE, build
-    build.build()
-    torch.cuda.set_device(0)
-    Ts = [int(t) for t in args.sweep.split(",")]
-    wl = C.workload("k3_sweep_t1")
-    cfg = wl.cfg
-    W = G.gen_weights(wl, device="cuda")
-    layer = LatentMoE(cfg, W, max_tokens=max(Ts))
-    pk = peaks()
-    A = accounting(cfg)
-    flops_per_token = A["flops_per_token"]
-    for T in Ts:
-        wlT = replace(wl, T=T, name=f"k3_sweep_t{T}")
-        xs = [G.gen_x(replace(wlT, seed=wl.seed + 7919 * (i + 1)), device="cuda") for i in range(4)]
-        out = torch.empty(T, cfg.d_model, dtype=torch.bfloat16, device="cuda")
-        U = []
-        for xb in xs:
-            layer.lmoe_forward(xb, out=out)
-            U.append(layer.lmoe_last_active_experts())
-        for i in range(max(args.warmup, 3)):
-            layer.lmoe_forward(xs[i % 4], out=out)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        layer.lmoe_forward(xs[0], out=out)
-        torch.cuda.synchronize()
-        est = time.perf_counter() - t0
-        steps = max(10, min(args.steps, int(0.5 / max(est, 1e-5))))
-        layer.lmoe_set_profiling(steps, stages=["expert_gate_up", "expert_down"])
-        layer.lmoe_set_profiling_period(PROFILE_PERIOD)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(steps):
-            layer.lmoe_forward(xs[i % 4], out=out)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        prof = layer.lmoe_profile_get()
-        n_prof = min(steps, 50)
-        layer.lmoe_set_profiling_period(1)
-        layer.lmoe_set_profiling(n_prof)
-        for i in range(n_prof):
-            layer.lmoe_forward(xs[i % 4], out=out)
-        stage_prof = layer.lmoe_profile_get()
-        layer.lmoe_set_profiling(0)
-        layer.lmoe_sync_status()
-        U_mean = sum(U[i % 4] for i in range(steps)) / steps
-        layer_bytes = A["dense"] + U_mean * A["expert"] + T * A["token_io"]
-        gu_bytes = U_mean * A["gu_w"]
-        dn_bytes = U_mean * A["dn_w"]
-        gu = prof["expert_gate_up"][0] / max(prof["expert_gate_up"][1], 1)
-        dn = prof["expert_down"][0] / max(prof["expert_down"][1], 1)
-        tflops = T * flops_per_token / (ms * 1e-3) / 1e12
-        print(json.dumps({
-            "workload": wlT.name, "T": T, "steps": steps, "tokens_per_s": round(T / (ms * 1e-3), 1),
-            "ms_per_step": round(ms, 4), "active_experts_mean": round(U_mean, 1),
-            "layer_hbm": {"bytes": int(layer_bytes), "gbs": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
-                          "frac": round(layer_bytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)},
-            "layer_tensor": {"tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / pk["bf16"], 4),
-                             "frac_of_bf16_sustained": round(tflops / pk["bf16_sus"], 4)},
-            "expert_gate_up_gbs": round(gu_bytes / (gu * 1e-3) / 1e9, 1),
-            "expert_down_gbs": round(dn_bytes / (dn * 1e-3) / 1e9, 1),
-            "stage_ms": {n: round(v[0] / max(v[1], 1), 4) for n, v in stage_prof.items()}}), flush=True)
-    layer.close()
 
 
 # ------------------------------------------------------------- reference
@@ -583,15 +654,12 @@ def main():
     ap.add_argument("--workload", default="k3_decode_t64")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=2)
-    ap.add_argument("--sweep", default=None,
-                    help="comma-separated token counts: one JSON line per T on one GPU (not the driver's contract)")
+    ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
+    ap.add_argument("--no-tc-peaks", action="store_true", help="skip the tensor-pipe peak measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
-        run_sweep(args)
-    elif args.impl == "reference":
+    if args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -169,7 +169,10 @@ LMOE_API lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T
  * anything is launched.  It calls no cudaMalloc, cudaFree or allocating
  * library routine.  The first call on each device looks up the array's
  * device address (cudaGetSymbolAddress) and caches it: make that first call
- * outside any stream capture.  All calls share the one array, so calls that
+ * outside any stream capture.  The cached address belongs to the device's
+ * primary context as it was then: after cudaDeviceReset (or anything else
+ * that destroys that context) the array may move, so such a process must
+ * not call this function again.  All calls share the one array, so calls that
  * overlap on the GPU (other streams, other threads) race and must be
  * serialised by the caller; no part of the array needs to start at zero
  * (every word a call reads is written earlier in the same call).  Expert ids
@@ -185,10 +188,31 @@ LMOE_API lmoe_status lmoe_dispatch_noalloc(const int32_t* topk_idx, int T, int k
  * it is y_routed), "u_hat" bf16 [T][l] (latent layers), "h_shared"
  * bf16 [T][Fs] (layers with a bf16 shared MLP), "y_shared" fp32 [T][d]
  * (FP8 layers, whose shared expert runs on the FP8 expert GEMMs), "counts"
- * int32 [E], "offsets" int32 [E+1], "perm" int32 [T*k].  `bytes` must
- * equal the tensor's size for the last T; a name the layer does not have
- * returns INVALID_ARG. */
+ * int32 [E], "offsets" int32 [E+1], "perm" int32 [T*k], "delta_f32" fp32
+ * [T][d] (Delta before its bf16 rounding; only while lmoe_keep_f32_output
+ * is on).  `bytes` must equal the tensor's size for the last T; a name the
+ * layer does not have returns INVALID_ARG. */
 LMOE_API lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t stream);
+
+/* While enabled (enable != 0), every lmoe_forward also stores Delta as fp32
+ * before it is rounded to bf16, readable as the "delta_f32" debug tensor:
+ * the same launches, each writing one fp32 value beside each bf16 one.  The
+ * K3 card's equations end in Delta itself; the bf16 output holds it to half
+ * a bf16 spacing, which this lets a test see past.  Enabling allocates a
+ * [max_tokens][d] fp32 buffer (device-synchronising); disabling frees it.
+ * Errors: INVALID_ARG (NULL handle), OOM, CUDA. */
+LMOE_API lmoe_status lmoe_keep_f32_output(lmoe_handle h, int enable);
+
+/* Test of the deferred-error path: launches one warp that waits on a
+ * barrier nothing ever arrives at, through the same bounded wait the layer's
+ * kernels use, with a wall-clock limit of limit_ns (1,000 ns .. 1 s).  The
+ * wait gives up, records a timeout in the handle's error flag and the kernel
+ * returns (it holds no TMA copy, MMA or tensor memory), so the next
+ * lmoe_sync_status returns LMOE_ERR_TIMEOUT and clears the flag; the
+ * handle stays usable.  The pages have no counterpart: the K3 card's code
+ * waits on no device barrier.  Errors: INVALID_ARG (NULL handle, limit out
+ * of range), CUDA (launch failure). */
+LMOE_API lmoe_status lmoe_selftest_timeout(lmoe_handle h, unsigned long long limit_ns, cudaStream_t stream);
 
 /* Synchronise `stream` and return the first deferred error: a CUDA error, a
  * kernel timeout (TIMEOUT) or an out-of-range expert index (INVALID_ARG).

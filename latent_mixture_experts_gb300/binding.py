@@ -24,7 +24,7 @@ EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lm
            "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_set_profiling",
            "lmoe_set_profiling_period",
            "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string",
-           "lmoe_dispatch_noalloc")
+           "lmoe_dispatch_noalloc", "lmoe_keep_f32_output", "lmoe_selftest_timeout", "lmoe_tc_peak")
 NOALLOC_MAX_ASSIGNMENTS = 65536
 NOALLOC_MAX_EXPERTS = 2048
 PROFILE_ALL_STAGES = 0x1FF
@@ -84,6 +84,9 @@ def load_library(path: str = LIB_PATH):
             "lmoe_destroy": (I, [P]),
             "lmoe_status_string": (ctypes.c_char_p, [I]),
             "lmoe_dispatch_noalloc": (I, [P, I, I, I, P, P, P, P]),
+            "lmoe_keep_f32_output": (I, [P, I]),
+            "lmoe_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
+            "lmoe_tc_peak": (I, [I, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double), P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -122,6 +125,17 @@ def lmoe_dispatch_noalloc(topk_idx: torch.Tensor, n_experts: int, counts: torch.
     T, k = topk_idx.shape
     _check("lmoe_dispatch_noalloc", load_library().lmoe_dispatch_noalloc(
         _ptr(topk_idx), T, k, int(n_experts), _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)))
+
+
+TC_KINDS = {"bf16": 0, "e4m3_e4m3": 1, "e2m1_e4m3": 2, "mxfp4": 3, "nvfp4": 4}
+
+
+def tc_peak(kind: str, iters: int, stream=None) -> float:
+    """Measured tensor-pipe rate (TFLOP/s) of one MMA form (include/lmoe_peak.h)."""
+    ms, fl = ctypes.c_float(), ctypes.c_double()
+    _check("lmoe_tc_peak", load_library().lmoe_tc_peak(TC_KINDS[kind], int(iters), ctypes.byref(ms),
+                                                       ctypes.byref(fl), _stream(stream)))
+    return fl.value / (ms.value * 1e-3) / 1e12
 
 
 def make_config(cfg, max_tokens: int) -> LmoeConfig:
@@ -204,13 +218,21 @@ class LatentMoE:
         shapes = {"logits": ((T, c.n_experts), torch.float32), "xc": ((T, c.d_latent), torch.float32),
                   "u": ((T, dx), torch.float32), "u_hat": ((T, dx), torch.bfloat16),
                   "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "y_shared": ((T, c.d_model), torch.float32),
-                  "counts": ((c.n_experts,), torch.int32),
+                  "delta_f32": ((T, c.d_model), torch.float32), "counts": ((c.n_experts,), torch.int32),
                   "offsets": ((c.n_experts + 1,), torch.int32), "perm": ((T * c.top_k,), torch.int32)}
         shape, dt = shapes[name]
         dst = torch.empty(shape, dtype=dt, device="cuda")
         _check("lmoe_debug_tensor", self._lib.lmoe_debug_tensor(self._h, name.encode(), _ptr(dst),
                                                                 dst.numel() * dst.element_size(), _stream(stream)))
         return dst
+
+    def lmoe_keep_f32_output(self, enable: bool = True):
+        """Keep Delta before its bf16 rounding (debug tensor "delta_f32")."""
+        _check("lmoe_keep_f32_output", self._lib.lmoe_keep_f32_output(self._h, int(bool(enable))))
+
+    def lmoe_selftest_timeout(self, limit_ns: int, stream=None):
+        """Launch the bounded-wait probe: the next lmoe_sync_status reports a timeout."""
+        _check("lmoe_selftest_timeout", self._lib.lmoe_selftest_timeout(self._h, int(limit_ns), _stream(stream)))
 
     def lmoe_sync_status(self, stream=None):
         _check("lmoe_sync_status", self._lib.lmoe_sync_status(self._h, _stream(stream)))

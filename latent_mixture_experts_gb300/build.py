@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "liblmoe.so")
-SOURCES = ["dense_gemm.cu", "routing.cu", "moe_gemm.cu", "moe_fp8.cu", "lmoe_api.cu", "dispatch_noalloc.cu"]
+SOURCES = ["dense_gemm.cu", "routing.cu", "moe_gemm.cu", "moe_fp8.cu", "lmoe_api.cu", "dispatch_noalloc.cu", "selftest.cu", "tc_peak.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
@@ -33,7 +33,7 @@ def _compile(src: str, verbose: bool) -> str:
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
-        os.path.join(HERE, "..", "include", "lmoe.h"), __file__]
+        os.path.join(HERE, "..", "include", "lmoe.h"), os.path.join(HERE, "..", "include", "lmoe_peak.h"), __file__]
     if not force and os.path.exists(LIB):
         newest = max(os.path.getmtime(p) for p in deps)
         if os.path.getmtime(LIB) >= newest:

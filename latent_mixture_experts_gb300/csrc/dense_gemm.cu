@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
         // direct bf16 result (one K split), plus the optional fp32 addend
         __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(p.out16) + out_row0 + mtl * 128 + 32 * warp + lane;
         const float* ad = p.add ? p.add + out_row0 + mtl * 128 + 32 * warp + lane : nullptr;
+        float* o32 = p.out32 ? p.out32 + out_row0 + mtl * 128 + 32 * warp + lane : nullptr;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = n0 + c0 + j;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
             float v = have ? __uint_as_float(r[j]) : 0.0f;
             if (ad) v += ad[static_cast<size_t>(t) * p.ld_add];
             o16[static_cast<size_t>(t) * p.ldo] = __float2bfloat16_rn(v);
+            if (o32) o32[static_cast<size_t>(t) * p.ldo] = v;
           }
         }
       } else if (row_ok) {
@@ -223,7 +225,7 @@ __global__ void finalize_sum_f32_kernel(const float* __restrict__ part, int spli
 
 __global__ void finalize_sum_bf16_kernel(const float* __restrict__ part, int splits, int T, int M, int ld,
                                          __nv_bfloat16* __restrict__ out, int ldo, const float* __restrict__ add,
-                                         int ld_add) {
+                                         int ld_add, float* __restrict__ out32) {
   griddep_launch();
   griddep_wait();
   const size_t n = static_cast<size_t>(T) * M;
@@ -235,6 +237,7 @@ __global__ void finalize_sum_bf16_kernel(const float* __restrict__ part, int spl
     for (int s = 0; s < splits; ++s) acc += part[s * plane + t * ld + m];
     if (add) acc += add[t * ld_add + m];
     out[t * ldo + m] = __float2bfloat16_rn(acc);
+    if (out32) out32[t * ldo + m] = acc;
   }
 }
 
@@ -325,11 +328,11 @@ cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M,
 }
 
 cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M, int ld, void* out, int ldo,
-                                     const float* add_opt, int ld_add, cudaStream_t s) {
+                                     const float* add_opt, int ld_add, float* out32_opt, cudaStream_t s) {
   const size_t n = static_cast<size_t>(T) * M;
   {
     const cudaError_t e_ = launch_ew(finalize_sum_bf16_kernel, n, s, part, splits, T, M, ld,
-                                     static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add);
+                                     static_cast<__nv_bfloat16*>(out), ldo, add_opt, ld_add, out32_opt);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();

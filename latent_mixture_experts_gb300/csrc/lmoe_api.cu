@@ -70,6 +70,7 @@ struct lmoe_ctx {
   void* h_s = nullptr;
   void* x_stage = nullptr;
   void* out_stage = nullptr;
+  float* delta32 = nullptr;   // Delta before its bf16 rounding, [Tm][d] (allocated by lmoe_keep_f32_output)
   uint8_t *sfa_gate = nullptr, *sfa_up = nullptr, *sfa_down = nullptr;
   const uint8_t *codes_gate = nullptr, *codes_up = nullptr, *codes_down = nullptr;
   uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
@@ -620,9 +621,29 @@ lmoe_status lmoe_destroy(lmoe_handle h) {
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_latent) cudaEventDestroy(h->ev_latent);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->delta32) cudaFree(h->delta32);
   cudaFree(h->pool);
   delete h;
   return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+lmoe_status lmoe_keep_f32_output(lmoe_handle h, int enable) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  if (enable && !h->delta32) {
+    LMOE_TRY(cudaDeviceSynchronize());
+    LMOE_TRY(cudaMalloc(&h->delta32, static_cast<size_t>(h->Tm) * h->d * sizeof(float)));
+  } else if (!enable && h->delta32) {
+    LMOE_TRY(cudaDeviceSynchronize());
+    LMOE_TRY(cudaFree(h->delta32));
+    h->delta32 = nullptr;
+  }
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_selftest_timeout(lmoe_handle h, unsigned long long limit_ns, cudaStream_t st) {
+  if (!h || limit_ns < 1000ull || limit_ns > 1000000000ull) return LMOE_ERR_INVALID_ARG;
+  LMOE_TRY(launch_wait_timeout_probe(h->err, limit_ns, st));
+  return LMOE_OK;
 }
 
 lmoe_status lmoe_route(lmoe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w, cudaStream_t st) {
@@ -921,11 +942,12 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     if (p.splits == 1) {   // one K split: the epilogue writes Delta in bf16
       p.epi = 1;
       p.out16 = out;
+      p.out32 = h->delta32;
       LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
       ++launches;
     } else {
       LMOE_TRY(launch_dense_gemm(p, p.mtiles0, BN, st));
-      LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, st));
+      LMOE_TRY(launch_finalize_sum_bf16(h->part, p.splits, T, d, d, out, d, nullptr, 0, h->delta32, st));
       launches += 2;
     }
     tm.done();
@@ -934,12 +956,12 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     StageTimer tm(h, LMOE_STAGE_OUTPUT, st);
     int splits = 0;
     if (Fs && h->fp8) {
-      LMOE_TRY(launch_finalize_sum_bf16(h->y_sh, 1, T, d, d, out, d, h->u, d, st));
+      LMOE_TRY(launch_finalize_sum_bf16(h->y_sh, 1, T, d, d, out, d, h->u, d, h->delta32, st));
       ++launches;
       splits = -1;
     }
     if (splits >= 0) {
-      LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, st));
+      LMOE_TRY(launch_finalize_sum_bf16(h->part, splits, T, d, d, out, d, h->u, d, h->delta32, st));
       ++launches;
     }
     tm.done();
@@ -989,6 +1011,10 @@ lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t
   } else if (!std::strcmp(name, "y_shared")) {
     if (!h->fp8 || !h->Fs) return LMOE_ERR_INVALID_ARG;
     src = h->y_sh;
+    want = T * h->d * 4;
+  } else if (!std::strcmp(name, "delta_f32")) {
+    if (!h->delta32) return LMOE_ERR_INVALID_ARG;
+    src = h->delta32;
     want = T * h->d * 4;
   } else if (!std::strcmp(name, "counts")) {
     src = h->counts;

@@ -31,6 +31,7 @@ struct DenseParams {
   // interleaved copy in a0w), bf16 out16[t][f] = act(gate, up), splits = 1.
   int epi;
   void* out16;
+  float* out32;           // epilogue 1: when set, also the fp32 value before the bf16 rounding, [t][row]
   const float* add;
   int ld_add;
   int act;
@@ -55,8 +56,9 @@ cudaError_t launch_interleave_gate_up(const void* gate, const void* up, int Fs, 
 // Sum `splits` partial planes [splits][T][ld] and apply an epilogue.
 cudaError_t launch_finalize_sum_f32(const float* part, int splits, int T, int M, int ld, float* out, int ldo,
                                     cudaStream_t s);
+// out32_opt: when set, also the fp32 sum before the bf16 rounding ([T][ldo]).
 cudaError_t launch_finalize_sum_bf16(const float* part, int splits, int T, int M, int ld, void* out, int ldo,
-                                     const float* add_opt, int ld_add, cudaStream_t s);
+                                     const float* add_opt, int ld_add, float* out32_opt, cudaStream_t s);
 // gate at columns [0, F), up at [F, 2F) of each partial row.
 cudaError_t launch_finalize_glu_bf16(const float* part, int splits, int T, int F, int ld, void* out, int act,
                                      float b1, float b2, cudaStream_t s);
@@ -226,6 +228,10 @@ cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s);
 // ks > 1: y holds ks planes (partials of a K-split down pass), plane elements apart, all added.
 cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, size_t plane, const void* norm_w,
                                 int use_norm, float eps, float* u, void* u_hat, int num_sms, cudaStream_t s);
+
+// One warp waits on an mbarrier nothing arrives at, with the given limit;
+// the bounded wait then records kErrTimeout in err[0].
+cudaError_t launch_wait_timeout_probe(int* err, unsigned long long limit_ns, cudaStream_t s);
 
 // Create-time repacking of the expert weights.
 cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,

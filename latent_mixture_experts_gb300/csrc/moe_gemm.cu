@@ -105,7 +105,10 @@ __device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t 
   }
   tc_fence_before();
   mbar_arrive(acc_empty);
+  // every lane's partial stores are fenced and the warp has converged before
+  // lane 0 announces them with the arrival counter
   __threadfence();
+  __syncwarp();
   int* const cnt = p.gcnt + static_cast<size_t>(wb) * 4 + q;
   int old = 0;
   if (lane == 0) old = atomicAdd(cnt, 1);
@@ -846,10 +849,18 @@ cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, siz
   if (T <= 0) return cudaSuccess;
   if (ks < 1 || plane % 4) return cudaErrorInvalidValue;
   const int per = (l / 4 + kCombineSlices - 1) / kCombineSlices;
-  if (T <= kCombineClusterMaxT && static_cast<size_t>(per) * sizeof(float4) <= 48 * 1024) {
-    int groups = kCombineMaxGroups;   // about one wave of CTAs, within 48 KB of group sums
+  // dynamic shared memory without opting in: 48 KB less the kernel's static arrays
+  static size_t dyn_limit = 0;
+  if (!dyn_limit) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, combine_norm_cluster_kernel);
+    if (e != cudaSuccess) return e;
+    dyn_limit = 48 * 1024 - fa.sharedSizeBytes;
+  }
+  if (T <= kCombineClusterMaxT && static_cast<size_t>(per) * sizeof(float4) <= dyn_limit) {
+    int groups = kCombineMaxGroups;   // about one wave of CTAs, within the group-sum budget
     while (groups > 1 && (static_cast<long long>(T) * kCombineSlices * groups > 2LL * num_sms ||
-                          static_cast<size_t>(groups) * per * sizeof(float4) > 48 * 1024))
+                          static_cast<size_t>(groups) * per * sizeof(float4) > dyn_limit))
       groups >>= 1;
     const size_t smem = static_cast<size_t>(groups) * per * sizeof(float4);
     const cudaError_t e_ = launch_pdl_cluster(combine_norm_cluster_kernel, dim3(kCombineSlices, T), kCombineLanes * groups,

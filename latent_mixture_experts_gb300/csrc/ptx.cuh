@@ -56,12 +56,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  Returns false (and
 // sets *err, if given, to `code`) when the wall-clock limit passes.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err = nullptr,
-                                          int code = 1) {
+                                          int code = 1, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       if (err) atomicExch(err, code);
       return false;
     }

@@ -72,6 +72,9 @@ WORKLOADS = {
 # Kimi-K3 shapes with 64 experts (1.1 GB of expert weights): the small case
 # for detailed profiler captures of the same kernels.
 WORKLOADS["k3_e64_t8"] = Workload("k3_e64_t8", replace(K3, n_experts=64), T=8, seed=6)
+# The same 64 experts at T = 1024 (256 assignments per expert): the prefill
+# token tile (96) on a case small enough for a full profiler capture.
+WORKLOADS["k3_e64_t1024"] = Workload("k3_e64_t1024", replace(K3, n_experts=64), T=1024, seed=7)
 # Kimi-K2 shapes with 32 experts (1.4 GB of FP8 expert weights) and 96
 # assignments per expert, near the 85 of the K2 T = 4096 batch.
 WORKLOADS["k2_e32_t384"] = Workload("k2_e32_t384", replace(K2, n_experts=32), T=384, seed=8)

@@ -10,12 +10,18 @@ import pytest
 from tests._harness import built_library
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "lmoe.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:LMOE_API\s+)?(?:lmoe_status|const char\s*\*|int)\s+(lmoe_\w+)\s*\(", text, re.M)))
+    """Every function any header under include/ declares."""
+    names = set()
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            text = open(os.path.join(INCLUDE, f)).read()
+            names.update(re.findall(r"^\s*(?:LMOE_API\s+)?(?:lmoe_status|const char\s*\*|int)\s+(lmoe_\w+)\s*\(",
+                                    text, re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +33,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_destroy"):
+    for must in ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_destroy", "lmoe_tc_peak"):
         assert must in names
 
 
@@ -105,6 +111,17 @@ def test_null_handle_calls(lib):
     assert lib.lmoe_sync_status(None, None) == b.LMOE_ERR_INVALID_ARG
     assert lib.lmoe_destroy(None) == b.LMOE_OK
     assert lib.lmoe_last_launch_count(None) == 0
+    assert lib.lmoe_keep_f32_output(None, 1) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_selftest_timeout(None, 5000, None) == b.LMOE_ERR_INVALID_ARG
+
+
+def test_tc_peak_rejects_bad_arguments(lib):
+    from latent_mixture_experts_gb300 import binding as b
+    ms, fl = ctypes.c_float(), ctypes.c_double()
+    assert lib.lmoe_tc_peak(9, 10, ctypes.byref(ms), ctypes.byref(fl), None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_tc_peak(0, 0, ctypes.byref(ms), ctypes.byref(fl), None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_tc_peak(0, (1 << 20) + 1, ctypes.byref(ms), ctypes.byref(fl), None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_tc_peak(0, 10, None, ctypes.byref(fl), None) == b.LMOE_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

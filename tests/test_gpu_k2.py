@@ -3,7 +3,7 @@ scale 2.827, SwiGLU experts on the full width, one shared expert, FP8 E4M3
 weights with fp32 scales per 128 x 128 block) with the fp64 oracle.
 
 A small K2-shaped layer is checked step by step and as a whole; the full K2
-workload (T = 4096) is checked on every token's routing and on sampled
+workload (T = 4096) is checked on every token's routing and on 16 sampled
 tokens' outputs."""
 from dataclasses import replace
 
@@ -13,8 +13,10 @@ import torch
 
 import oracle as O
 from lmoe_inputs import configs as C
-from tests._harness import assert_delta_close, gpu_inputs, make_layer, oracle_layer, rel_l2_per_token, x_bits
-from tests.test_gpu_parity import _check_routes
+from tests._harness import (assert_delta_close, forward_checked, gpu_inputs, make_layer, oracle_layer,
+                            rel_l2_per_token, x_bits)
+from tests._oracle_workers import OracleWorkers
+from tests.test_gpu_parity import _check_routes, full_size_check
 
 pytestmark = pytest.mark.gpu
 
@@ -32,11 +34,8 @@ def k2_small():
 def test_k2_small_steps_and_layer(k2_small):
     wl, W, x, layer, olayer = k2_small
     T = x.shape[0]
-    out, idx, Gw = layer.lmoe_forward(x, return_routing=True)
-    torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    idx = idx.cpu().numpy()
-    r = _check_routes(wl, layer, olayer, x, idx, Gw.cpu().numpy())
+    got, got32, idx, Gw = forward_checked(layer, x)
+    r = _check_routes(wl, layer, olayer, x, idx, Gw)
     assert np.allclose(r["G"].sum(1), 2.827)
     ref = O.forward(olayer, x_bits(x), idx=idx)
     d = O.dispatch(idx, wl.cfg.n_experts)
@@ -45,7 +44,7 @@ def test_k2_small_steps_and_layer(k2_small):
     assert rel_l2_per_token(u, ref["y_routed"]).max() <= 1e-2
     ys = layer.lmoe_debug_tensor("y_shared", T).cpu().double().numpy()   # shared expert on the FP8 GEMMs
     assert rel_l2_per_token(ys, ref["y_shared"]).max() <= 1e-2
-    assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+    assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
 
 
 def test_k2_small_token_tiles(k2_small):
@@ -53,25 +52,22 @@ def test_k2_small_token_tiles(k2_small):
     the oracle; repeated forwards are bit-identical."""
     wl, W, x, layer, olayer = k2_small
     for T in (1, 7):
-        out = layer.lmoe_forward(x[:T].contiguous())
+        got, got32, _, _ = forward_checked(layer, x[:T].contiguous())
         ref = O.forward(olayer, x_bits(x[:T]))
-        assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+        assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
     a = layer.lmoe_forward(x).cpu()
     b = layer.lmoe_forward(x).cpu()
     assert torch.equal(a, b)
 
 
 def test_k2_full_size():
+    """The K2 workload (T = 4096, seed 3): every token's routing, Delta on 16
+    sampled tokens."""
     wl = C.workload("k2_t4096")
     W, x = gpu_inputs(wl)
     layer = make_layer(wl, W, max_tokens=wl.T)
-    olayer = oracle_layer(wl, W)
-    out, idx, Gw = layer.lmoe_forward(x, return_routing=True)
-    torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    idx = idx.cpu().numpy()
-    sample = [0, 1000, 2047, 4095]
-    _check_routes(wl, layer, olayer, x, idx, Gw.cpu().numpy(), tokens=sample)
-    ref = O.forward(olayer, x_bits(x)[sample], idx=idx[sample])
-    assert_delta_close(out.cpu().double().numpy()[sample], ref["delta"])
-    layer.close()
+    try:
+        with OracleWorkers(wl, W) as workers:
+            full_size_check(wl, layer, oracle_layer(wl, W), workers, x)
+    finally:
+        layer.close()

@@ -7,8 +7,13 @@ Each step of the hot path is checked on its own, then the whole layer:
   h, and Delta at the layer tolerances (per-token relative L2 <= 1e-2,
   max-abs <= 2e-2 * RMS(Delta)).
 Workloads: the tiny layer, a mid-size layer whose every GEMM spans several
-tiles with ragged tails (and K padding in the expert GEMMs), the full
-Kimi-K3 decode batch and the full prefill batch (sampled tokens).
+tiles with ragged tails (and K padding in the expert GEMMs), and every
+full-size Kimi-K3 configuration: the decode batch (T = 64, seed 1), the
+token-count sweep (T = 8 .. 2048, seed 4) and the Zipf-skewed prefill batch
+(T = 8192, seed 2), each with every token's routing checked and Delta on
+every token (T <= 16) or 16 sampled ones.  The max-abs bound applies to
+Delta before its final bf16 rounding (the forward keeps that fp32 value as
+a debug tensor); the bf16 output's own raw figure is printed beside it.
 """
 from dataclasses import replace
 
@@ -19,8 +24,9 @@ import torch
 import oracle as O
 from lmoe_inputs import configs as C
 from lmoe_inputs import generate as G
-from tests._harness import (assert_delta_close, gpu_inputs, make_layer, oracle_layer, rel_l2_per_token,
-                            valid_selection, x_bits)
+from tests._harness import (assert_delta_close, forward_checked, gpu_inputs, make_layer, oracle_layer,
+                            rel_l2_per_token, sample_tokens, valid_selection, x_bits)
+from tests._oracle_workers import OracleWorkers
 
 pytestmark = pytest.mark.gpu
 
@@ -134,11 +140,8 @@ def test_dispatch_rejects_out_of_range_expert(tiny):
 def test_steps_and_layer(which, request):
     wl, W, x, layer, olayer = request.getfixturevalue(which)
     T = x.shape[0]
-    out, idx, Gw = layer.lmoe_forward(x, return_routing=True)
-    torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    idx = idx.cpu().numpy()
-    _check_routes(wl, layer, olayer, x, idx, Gw.cpu().numpy())
+    got, got32, idx, Gw = forward_checked(layer, x)
+    _check_routes(wl, layer, olayer, x, idx, Gw)
     ref = O.forward(olayer, x_bits(x), idx=idx)          # oracle run with the GPU's selection
     # latent down-projection (fp32 accumulation of bf16 products)
     xc = layer.lmoe_debug_tensor("xc", T).cpu().double().numpy()
@@ -156,17 +159,34 @@ def test_steps_and_layer(which, request):
     hs = layer.lmoe_debug_tensor("h_shared", T).cpu().double().numpy()
     assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
     # the layer
-    assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+    assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
+
+
+def test_f32_output_leaves_the_bf16_output_unchanged(mid):
+    """Keeping the fp32 Delta adds stores only: the bf16 output of a handle
+    without it is bit-identical."""
+    wl, W, x, layer, olayer = mid
+    plain = make_layer(wl, W, max_tokens=256, keep_f32=False)
+    try:
+        a = plain.lmoe_forward(x).cpu()
+        b = layer.lmoe_forward(x).cpu()
+        plain.lmoe_sync_status()
+        assert torch.equal(a, b)
+        from latent_mixture_experts_gb300 import LmoeError
+        with pytest.raises(LmoeError):
+            plain.lmoe_debug_tensor("delta_f32", x.shape[0])
+    finally:
+        plain.close()
 
 
 def test_ragged_T_and_edge_cases(mid):
     wl, W, x, layer, olayer = mid
     full = layer.lmoe_forward(x).cpu()
     for T in (1, 37):
-        out = layer.lmoe_forward(x[:T].contiguous())
-        torch.cuda.synchronize()
+        got, got32, idx, _ = forward_checked(layer, x[:T].contiguous())
+        out = torch.from_numpy(got).to(torch.bfloat16)
         ref = O.forward(olayer, x_bits(x[:T]))
-        assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+        assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
         # per-token independence: the first T rows do not depend on the others
         assert torch.equal(out.cpu(), full[:T]) or \
             rel_l2_per_token(out.cpu().double().numpy(), full[:T].double().numpy()).max() < 1e-2
@@ -219,30 +239,60 @@ def test_generator_bytes_match_cpu():
     assert torch.equal(G.gen_x(wl, "cpu"), G.gen_x(wl, "cuda").cpu())
 
 
+def test_bounded_wait_reports_timeout(tiny):
+    """A kernel waiting on a barrier nothing arrives at gives up after its
+    limit: the next status check reports the timeout and clears it, and the
+    handle keeps working."""
+    wl, W, x, layer, olayer = tiny
+    from latent_mixture_experts_gb300 import LmoeError, LMOE_ERR_INVALID_ARG, LMOE_ERR_TIMEOUT
+    before = layer.lmoe_forward(x).cpu()
+    layer.lmoe_sync_status()
+    layer.lmoe_selftest_timeout(5_000)              # 5 us
+    with pytest.raises(LmoeError) as ei:
+        layer.lmoe_sync_status()
+    assert ei.value.status == LMOE_ERR_TIMEOUT
+    layer.lmoe_sync_status()                          # flag cleared
+    assert torch.equal(layer.lmoe_forward(x).cpu(), before)
+    layer.lmoe_sync_status()
+    for bad in (10, 2_000_000_000):
+        with pytest.raises(LmoeError) as ei:
+            layer.lmoe_selftest_timeout(bad)
+        assert ei.value.status == LMOE_ERR_INVALID_ARG
+
+
+def full_size_check(wl, layer, olayer, workers, x, n_sample=16, seed=0):
+    """Every token's routing against the oracle (indices bit-exact, near
+    ties flagged and checked for validity), then Delta on every token (T <=
+    n_sample) or n_sample tokens including flagged ones and one on the most
+    loaded expert, computed by the oracle with the GPU's selection."""
+    T = x.shape[0]
+    got, got32, idx, Gw = forward_checked(layer, x)
+    r = _check_routes(wl, layer, olayer, x, idx, Gw)
+    sample = sample_tokens(T, n_sample, r, idx, seed)
+    ref = workers.forward(x_bits(x)[sample], idx[sample])
+    assert_delta_close(got[sample], ref["delta"], got32[sample],
+                       label=f"{wl.name} T={T} ({len(sample)} tokens, {int(r['flag'].sum())} flagged)")
+    return got, idx
+
+
 @pytest.fixture(scope="module")
 def k3_decode():
     wl = C.workload("k3_decode_t64")
     W, x = gpu_inputs(wl)
     layer = make_layer(wl, W, max_tokens=wl.T)
-    yield wl, W, x, layer, oracle_layer(wl, W)
+    workers = OracleWorkers(wl, W)
+    yield wl, W, x, layer, oracle_layer(wl, W), workers
+    workers.close()
     layer.close()
     del W
     torch.cuda.empty_cache()
 
 
 def test_k3_decode_full_size(k3_decode):
-    """Kimi-K3 shapes, T = 64, in the launch configuration the benchmark
-    times: routing of every token against the oracle, Delta on sampled
-    tokens the oracle computes one by one."""
-    wl, W, x, layer, olayer = k3_decode
-    out, idx, Gw = layer.lmoe_forward(x, return_routing=True)
-    torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    idx = idx.cpu().numpy()
-    _check_routes(wl, layer, olayer, x, idx, Gw.cpu().numpy())
-    sample = [0, 17, 42, 63]
-    ref = O.forward(olayer, x_bits(x)[sample], idx=idx[sample])
-    assert_delta_close(out.cpu().double().numpy()[sample], ref["delta"])
+    """Kimi-K3 shapes, T = 64, seed 1, in the launch configuration the
+    benchmark times."""
+    wl, W, x, layer, olayer, workers = k3_decode
+    full_size_check(wl, layer, olayer, workers, x)
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4])
@@ -252,36 +302,46 @@ def test_k3_small_batch_k_split(k3_decode, T):
     last split to arrive, down partials added by the combine): every token
     against the oracle, and repeated forwards bit-identical (the partials are
     added in split order whatever the arrival order)."""
-    wl, W, x, layer, olayer = k3_decode
+    wl, W, x, layer, olayer, workers = k3_decode
     xs = x[:T].contiguous()
-    out, idx, Gw = layer.lmoe_forward(xs, return_routing=True)
+    got, idx = full_size_check(wl, layer, olayer, workers, xs)
     again = layer.lmoe_forward(xs)
     torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    assert torch.equal(out, again)
-    idx = idx.cpu().numpy()
-    _check_routes(wl, layer, olayer, xs, idx, Gw.cpu().numpy())
-    ref = O.forward(olayer, x_bits(xs), idx=idx)
-    assert_delta_close(out.cpu().double().numpy(), ref["delta"])
+    assert np.array_equal(again.cpu().double().numpy(), got)
+
+
+@pytest.fixture(scope="module")
+def k3_sweep():
+    """The token-count sweep configuration: Kimi-K3 shapes, seed 4, uniform
+    bias; one layer serves every T (the tokens of a smaller T are the first
+    rows of the largest batch)."""
+    wl = C.workload("k3_sweep_t2048")
+    W, x = gpu_inputs(wl)
+    layer = make_layer(wl, W, max_tokens=wl.T)
+    workers = OracleWorkers(wl, W)
+    yield wl, W, x, layer, oracle_layer(wl, W), workers
+    workers.close()
+    layer.close()
+    del W
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [8, 32, 128, 512, 2048])
+def test_k3_sweep_full_size(k3_sweep, T):
+    wl, W, x, layer, olayer, workers = k3_sweep
+    assert torch.equal(x[:T].cpu(), G.gen_x(C.workload(f"k3_sweep_t{T}"), "cpu"))
+    full_size_check(replace(wl, T=T, name=f"k3_sweep_t{T}"), layer, olayer, workers, x[:T].contiguous(), seed=T)
 
 
 def test_k3_prefill_full_size():
-    """T = 8192 with the Zipf-skewed bias: every token's routing checked
-    for validity, sampled tokens (one on the most loaded expert) against
-    the oracle."""
+    """T = 8192 with the Zipf-skewed bias (seed 2): every token's routing,
+    Delta on 16 sampled tokens (flagged ones and one on the most loaded
+    expert among them)."""
     wl = C.workload("k3_prefill_t8192")
     W, x = gpu_inputs(wl)
     layer = make_layer(wl, W, max_tokens=wl.T)
-    olayer = oracle_layer(wl, W)
-    out, idx, Gw = layer.lmoe_forward(x, return_routing=True)
-    torch.cuda.synchronize()
-    layer.lmoe_sync_status()
-    idx = idx.cpu().numpy()
-    counts = np.bincount(idx.reshape(-1), minlength=wl.cfg.n_experts)
-    hot = int(np.argmax(counts))
-    t_hot = int(np.nonzero((idx == hot).any(1))[0][0])
-    sample = sorted({0, 4095, 8191, t_hot})
-    _check_routes(wl, layer, olayer, x, idx, Gw.cpu().numpy(), tokens=sample)
-    ref = O.forward(olayer, x_bits(x)[sample], idx=idx[sample])
-    assert_delta_close(out.cpu().double().numpy()[sample], ref["delta"])
-    layer.close()
+    try:
+        with OracleWorkers(wl, W) as workers:
+            full_size_check(wl, layer, oracle_layer(wl, W), workers, x)
+    finally:
+        layer.close()

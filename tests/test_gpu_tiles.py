@@ -13,7 +13,8 @@ import torch
 
 import oracle as O
 from lmoe_inputs import configs as C
-from tests._harness import assert_delta_close, gpu_inputs, make_layer, oracle_layer, rel_l2_per_token, x_bits
+from tests._harness import (assert_delta_close, forward_checked, gpu_inputs, make_layer, oracle_layer,
+                            rel_l2_per_token, x_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,17 +35,11 @@ def test_all_token_tiles(wl, Ts):
     try:
         for T in Ts:
             xt = x[:T].contiguous()
-            out, idx, _ = layer.lmoe_forward(xt, return_routing=True)
-            torch.cuda.synchronize()
-            layer.lmoe_sync_status()
-            idx = idx.cpu().numpy()
+            got, got32, idx, _ = forward_checked(layer, xt)
             ref = O.forward(olayer, x_bits(xt), idx=idx)
             u = layer.lmoe_debug_tensor("u", T).cpu().double().numpy()
             assert rel_l2_per_token(u, ref["u"]).max() <= 1e-2, T
-            got = out.cpu().double().numpy()
-            rel, beyond = assert_delta_close(got, ref["delta"])
-            raw = np.abs(got - ref["delta"]).max() / np.sqrt((ref["delta"] ** 2).mean())
-            print(f"{wl.name} T={T}: rel-L2 max {rel:.2e}, max-abs/RMS {raw:.2e} raw, {beyond:.2e} beyond bf16 rounding")
+            assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
         # repeated forwards of the largest batch are bit-identical
         a = layer.lmoe_forward(x).cpu()
         b = layer.lmoe_forward(x).cpu()
@@ -74,10 +69,7 @@ def test_wide_dense_tiles_all_tokens(wl):
     layer = make_layer(wl, W, max_tokens=wl.T)
     olayer = oracle_layer(wl, W)
     try:
-        out, idx, _ = layer.lmoe_forward(x, return_routing=True)
-        torch.cuda.synchronize()
-        layer.lmoe_sync_status()
-        idx = idx.cpu().numpy()
+        got, got32, idx, _ = forward_checked(layer, x)
         ref = O.forward(olayer, x_bits(x), idx=idx)
         if wl.cfg.expert_wfmt == "mxfp4":
             hs = layer.lmoe_debug_tensor("h_shared", wl.T).cpu().double().numpy()
@@ -85,8 +77,7 @@ def test_wide_dense_tiles_all_tokens(wl):
         else:
             ys = layer.lmoe_debug_tensor("y_shared", wl.T).cpu().double().numpy()
             assert rel_l2_per_token(ys, ref["y_shared"]).max() <= 1e-2
-        rel, beyond = assert_delta_close(out.cpu().double().numpy(), ref["delta"])
-        print(f"{wl.name} T={wl.T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
+        assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={wl.T}")
     finally:
         layer.close()
 
@@ -105,15 +96,12 @@ def test_split_k_dense_all_tokens():
     try:
         for T in (8, 64):
             xt = x[:T].contiguous()
-            out, idx, _ = layer.lmoe_forward(xt, return_routing=True)
-            torch.cuda.synchronize()
-            layer.lmoe_sync_status()
-            ref = O.forward(olayer, x_bits(xt), idx=idx.cpu().numpy())
+            got, got32, idx, _ = forward_checked(layer, xt)
+            ref = O.forward(olayer, x_bits(xt), idx=idx)
             xc = layer.lmoe_debug_tensor("xc", T).cpu().double().numpy()
             assert np.abs(xc - ref["xc"]).max() <= 1e-4 * (1 + np.abs(ref["xc"]).max())
             hs = layer.lmoe_debug_tensor("h_shared", T).cpu().double().numpy()
             assert rel_l2_per_token(hs, ref["h_s"]).max() <= 1e-2
-            rel, beyond = assert_delta_close(out.cpu().double().numpy(), ref["delta"])
-            print(f"{wl.name} T={T}: rel-L2 max {rel:.2e}, max-abs/RMS beyond bf16 rounding {beyond:.2e}")
+            assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")
     finally:
         layer.close()

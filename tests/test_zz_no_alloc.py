@@ -42,6 +42,27 @@ def test_noalloc_dispatch_matches_handle_dispatch():
     layer.close()
 
 
+@pytest.mark.parametrize("E,k,P", [(2048, 8, 8192), (2048, 8, 65536), (896, 16, 65536), (896, 16, 1024)],
+                         ids=["E2048_one_block", "E2048_max", "k3_max", "k3_t64"])
+def test_noalloc_dispatch_at_the_limits(E, k, P):
+    """Sizes at the documented limits (2048 experts; 65,536 assignments, the
+    largest batch; 8,192, the largest the one-kernel dispatch takes) and the
+    Kimi-K3 routing shape, bit for bit against the oracle's counting sort."""
+    import oracle as O
+    from latent_mixture_experts_gb300 import binding
+    T = P // k
+    idx = _idx(T, k, E, seed=P + E).cuda()
+    counts = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    perm = torch.full((P,), -1, dtype=torch.int32, device="cuda")
+    binding.lmoe_dispatch_noalloc(idx, E, counts, offsets, perm)
+    torch.cuda.synchronize()
+    d = O.dispatch(idx.cpu().numpy(), E)
+    assert np.array_equal(counts.cpu().numpy(), d["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), d["offsets"])
+    assert np.array_equal(perm.cpu().numpy(), d["perm"])
+
+
 def test_noalloc_dispatch_rejects_oversize():
     from latent_mixture_experts_gb300 import binding
     from latent_mixture_experts_gb300 import LmoeError, LMOE_ERR_INVALID_ARG
