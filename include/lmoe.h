@@ -182,6 +182,43 @@ LMOE_API lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T
 LMOE_API lmoe_status lmoe_dispatch_noalloc(const int32_t* topk_idx, int T, int k, int n_experts, int32_t* counts,
                                            int32_t* offsets, int32_t* perm, cudaStream_t stream);
 
+/* Quantile Balancing: the selection-bias update of Stable LatentMoE (tutorial
+ * "Stable LatentMoE", section "Quantile Balancing: giving every expert a
+ * fair shot"; walk-through "Kimi K3 模型结构（5）", section "Stable 之三：
+ * Quantile Balancing", appendices C and D).  For a batch of T tokens routed
+ * with biases b: alpha_t = token t's (k+1)-th largest biased score
+ * sigmoid(z_t) + b; r_tj = alpha_t - sigmoid(z_tj), the bias expert j needs to
+ * enter t's top-k.  The new biases are stored for the next batch; the batch
+ * itself keeps the biases it was routed with.
+ *
+ * Inputs of all three calls: logits fp32 [T][E] (the router's z; NULL = those
+ * of the handle's last lmoe_forward, whose T must then be passed), bias fp32
+ * [E] (the biases the batch was routed with; NULL = the handle's
+ * router_bias).  E and k are the handle's; k < E is required.  Stream-ordered,
+ * no host synchronisation.  Errors: INVALID_ARG (NULL handle or output, T out
+ * of [1, max_tokens], bins out of [1, 2^20], k >= E), CUDA.
+ *
+ * lmoe_qb_update (exact): new_bias fp32 [E] = q_j - mean(q), q_j = the
+ * (k/E)-quantile of r_{:,j} with the "higher" convention (the sorted value at
+ * index ceil(k (T-1) / E)). */
+LMOE_API lmoe_status lmoe_qb_update(lmoe_handle h, const float* logits, int T, const float* bias, float* new_bias,
+                                    cudaStream_t stream);
+/* lmoe_qb_histogram (appendix D): adds the batch's T x E required biases to
+ * counts int32 [E][bins], bins uniform over [min b - 1, max b + 1] (values
+ * outside go to the end bins).  The caller zeroes counts at the start of a
+ * step; calls for several micro-batches add up, and counts of several ranks
+ * add with one integer all-reduce (the bias, hence the range, must be the
+ * same on all of them). */
+LMOE_API lmoe_status lmoe_qb_histogram(lmoe_handle h, const float* logits, int T, const float* bias, int bins,
+                                       int32_t* counts, cudaStream_t stream);
+/* lmoe_qb_update_from_histogram: new_bias fp32 [E] from accumulated counts:
+ * per expert, m = its total count, target = ceil(m k / E); the first bin c
+ * whose cumulative count reaches the target, value = lo + w (c + (target -
+ * count before c) / count of c); then the mean is subtracted.  bias: the
+ * biases the counts were taken with (for the range). */
+LMOE_API lmoe_status lmoe_qb_update_from_histogram(lmoe_handle h, const int32_t* counts, int bins, const float* bias,
+                                                   float* new_bias, cudaStream_t stream);
+
 /* Copy an intermediate of the last lmoe_forward on this handle out of the
  * workspace (stream-ordered): "logits" fp32 [T][E] (router z), "xc" fp32
  * [T][l], "u" fp32 [T][l] (expert sum; [T][d] for non-latent layers, where

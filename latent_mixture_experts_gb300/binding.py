@@ -24,7 +24,8 @@ EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lm
            "lmoe_debug_tensor", "lmoe_sync_status", "lmoe_last_launch_count", "lmoe_set_profiling",
            "lmoe_set_profiling_period",
            "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string",
-           "lmoe_dispatch_noalloc", "lmoe_keep_f32_output", "lmoe_selftest_timeout", "lmoe_tc_peak")
+           "lmoe_dispatch_noalloc", "lmoe_keep_f32_output", "lmoe_selftest_timeout", "lmoe_tc_peak",
+           "lmoe_qb_update", "lmoe_qb_histogram", "lmoe_qb_update_from_histogram")
 NOALLOC_MAX_ASSIGNMENTS = 65536
 NOALLOC_MAX_EXPERTS = 2048
 PROFILE_ALL_STAGES = 0x1FF
@@ -87,6 +88,9 @@ def load_library(path: str = LIB_PATH):
             "lmoe_keep_f32_output": (I, [P, I]),
             "lmoe_selftest_timeout": (I, [P, ctypes.c_ulonglong, P]),
             "lmoe_tc_peak": (I, [I, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double), P]),
+            "lmoe_qb_update": (I, [P, P, I, P, P, P]),
+            "lmoe_qb_histogram": (I, [P, P, I, P, I, P, P]),
+            "lmoe_qb_update_from_histogram": (I, [P, P, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -233,6 +237,26 @@ class LatentMoE:
     def lmoe_selftest_timeout(self, limit_ns: int, stream=None):
         """Launch the bounded-wait probe: the next lmoe_sync_status reports a timeout."""
         _check("lmoe_selftest_timeout", self._lib.lmoe_selftest_timeout(self._h, int(limit_ns), _stream(stream)))
+
+    def lmoe_qb_update(self, T: int, logits=None, bias=None, stream=None) -> torch.Tensor:
+        """Exact Quantile Balancing update (new biases, fp32 [E]) for a batch
+        of T tokens: the given logits [T][E], or the last forward's."""
+        nb = torch.empty(self.cfg.n_experts, dtype=torch.float32, device="cuda")
+        _check("lmoe_qb_update", self._lib.lmoe_qb_update(self._h, _ptr(logits), int(T), _ptr(bias), _ptr(nb),
+                                                          _stream(stream)))
+        return nb
+
+    def lmoe_qb_histogram(self, T: int, counts: torch.Tensor, logits=None, bias=None, stream=None):
+        """Add a batch's required biases to counts (int32 [E][bins])."""
+        _check("lmoe_qb_histogram", self._lib.lmoe_qb_histogram(self._h, _ptr(logits), int(T), _ptr(bias),
+                                                                counts.shape[1], _ptr(counts), _stream(stream)))
+        return counts
+
+    def lmoe_qb_update_from_histogram(self, counts: torch.Tensor, bias=None, stream=None) -> torch.Tensor:
+        nb = torch.empty(self.cfg.n_experts, dtype=torch.float32, device="cuda")
+        _check("lmoe_qb_update_from_histogram", self._lib.lmoe_qb_update_from_histogram(
+            self._h, _ptr(counts), counts.shape[1], _ptr(bias), _ptr(nb), _stream(stream)))
+        return nb
 
     def lmoe_sync_status(self, stream=None):
         _check("lmoe_sync_status", self._lib.lmoe_sync_status(self._h, _stream(stream)))

@@ -71,6 +71,7 @@ struct lmoe_ctx {
   void* x_stage = nullptr;
   void* out_stage = nullptr;
   float* delta32 = nullptr;   // Delta before its bf16 rounding, [Tm][d] (allocated by lmoe_keep_f32_output)
+  float *qb_alpha = nullptr, *qb_raw = nullptr, *qb_range = nullptr;   // quantile-balancing scratch
   uint8_t *sfa_gate = nullptr, *sfa_up = nullptr, *sfa_down = nullptr;
   const uint8_t *codes_gate = nullptr, *codes_up = nullptr, *codes_down = nullptr;
   uint8_t *pad_gate = nullptr, *pad_up = nullptr, *pad_down = nullptr;
@@ -511,6 +512,9 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
       h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
     }
     if (pad_dn) h->pad_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->din * (h->Fp / 2), base);
+    h->qb_alpha = c.take<float>(h->Tm, base);
+    h->qb_raw = c.take<float>(h->E, base);
+    h->qb_range = c.take<float>(2, base);
     h->gpart = c.take<float>(static_cast<size_t>(gpart_elems), base);
     h->gcnt = c.take<int>(static_cast<size_t>(std::max(h->n_gcnt, 1)), base);
     return c.off;
@@ -637,6 +641,45 @@ lmoe_status lmoe_keep_f32_output(lmoe_handle h, int enable) {
     LMOE_TRY(cudaFree(h->delta32));
     h->delta32 = nullptr;
   }
+  return LMOE_OK;
+}
+
+// Inputs of a quantile-balancing call: the given logits, or those of the
+// handle's last forward (T must then be its token count), and the given
+// biases or the handle's router bias.
+static lmoe_status qb_inputs(lmoe_ctx* h, const float*& logits, int T, const float*& bias) {
+  if (T < 1 || T > h->Tm || h->k >= h->E) return LMOE_ERR_INVALID_ARG;
+  if (!logits) {
+    if (T != h->last_T) return LMOE_ERR_INVALID_ARG;
+    logits = h->logits;
+  }
+  if (!bias) bias = h->w.router_bias;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_qb_update(lmoe_handle h, const float* logits, int T, const float* bias, float* new_bias,
+                           cudaStream_t st) {
+  if (!h || !new_bias) return LMOE_ERR_INVALID_ARG;
+  const lmoe_status s = qb_inputs(h, logits, T, bias);
+  if (s != LMOE_OK) return s;
+  LMOE_TRY(launch_qb_update(logits, T, h->E, h->k, bias, h->qb_alpha, h->qb_raw, new_bias, st));
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_qb_histogram(lmoe_handle h, const float* logits, int T, const float* bias, int bins,
+                              int32_t* counts, cudaStream_t st) {
+  if (!h || !counts || bins < 1 || bins > (1 << 20)) return LMOE_ERR_INVALID_ARG;
+  const lmoe_status s = qb_inputs(h, logits, T, bias);
+  if (s != LMOE_OK) return s;
+  LMOE_TRY(launch_qb_histogram(logits, T, h->E, h->k, bias, bins, h->qb_alpha, h->qb_range, counts, st));
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_qb_update_from_histogram(lmoe_handle h, const int32_t* counts, int bins, const float* bias,
+                                          float* new_bias, cudaStream_t st) {
+  if (!h || !counts || !new_bias || bins < 1 || bins > (1 << 20) || h->k >= h->E) return LMOE_ERR_INVALID_ARG;
+  if (!bias) bias = h->w.router_bias;
+  LMOE_TRY(launch_qb_from_histogram(counts, h->E, bins, h->k, bias, h->qb_range, h->qb_raw, new_bias, st));
   return LMOE_OK;
 }
 

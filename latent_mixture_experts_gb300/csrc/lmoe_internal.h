@@ -229,6 +229,20 @@ cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t s);
 cudaError_t launch_combine_norm(const float* y, int T, int k, int l, int ks, size_t plane, const void* norm_w,
                                 int use_norm, float eps, float* u, void* u_hat, int num_sms, cudaStream_t s);
 
+// ------------------------------------------------------ quantile balancing
+// Exact update: alpha [T] (scratch) = each token's (k+1)-th largest biased
+// score, raw [E] (scratch) = the (k/E)-quantile of alpha_i - s_ij per expert,
+// new_bias = raw - mean(raw).  z: router logits fp32 [T][E].
+cudaError_t launch_qb_update(const float* z, int T, int E, int k, const float* bias, float* alpha, float* raw,
+                             float* new_bias, cudaStream_t s);
+// Adds the batch's required biases to counts [E][bins] (int32) over the range
+// [min b - 1, max b + 1] (written to range [2]).
+cudaError_t launch_qb_histogram(const float* z, int T, int E, int k, const float* bias, int bins, float* alpha,
+                                float* range, int32_t* counts, cudaStream_t s);
+// new_bias from the accumulated counts (quantile per expert, centred).
+cudaError_t launch_qb_from_histogram(const int32_t* counts, int E, int bins, int k, const float* bias, float* range,
+                                     float* raw, float* new_bias, cudaStream_t s);
+
 // One warp waits on an mbarrier nothing arrives at, with the given limit;
 // the bounded wait then records kErrTimeout in err[0].
 cudaError_t launch_wait_timeout_probe(int* err, unsigned long long limit_ns, cudaStream_t s);

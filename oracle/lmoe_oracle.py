@@ -321,3 +321,86 @@ def numpy_inputs(tensors: dict) -> dict:
         else:
             out[k] = v.numpy()
     return out
+
+
+# ------------------------------------------------------- quantile balancing
+# The selection-bias update of Stable LatentMoE (tutorial "Stable LatentMoE",
+# section "Quantile Balancing: giving every expert a fair shot"; walk-through
+# "Kimi K3 模型结构（5）", section "Stable 之三：Quantile Balancing", with its
+# appendix-C derivation and the appendix-D histogram estimator).  Scores s are
+# the raw sigmoids [m, n] of a batch routed with the current biases b.
+def qb_cutoffs(s: np.ndarray, b: np.ndarray, k: int) -> np.ndarray:
+    """alpha_i: the (k+1)-th largest biased score s_i + b of token i, the
+    line an expert must cross to enter token i's top-k."""
+    c = np.asarray(s, dtype=np.float64) + np.asarray(b, dtype=np.float64)[None, :]
+    assert k < c.shape[1], "the cutoff needs k + 1 <= n experts"
+    return -np.sort(-c, axis=1)[:, k]
+
+
+def qb_required_bias(s: np.ndarray, b: np.ndarray, k: int) -> np.ndarray:
+    """r_ij = alpha_i - s_ij: the bias expert j would need to cross token i's
+    cutoff (token i selects j under a new bias b_j exactly when b_j > r_ij)."""
+    return qb_cutoffs(s, b, k)[:, None] - np.asarray(s, dtype=np.float64)
+
+
+def quantile_higher(v: np.ndarray, num: int, den: int) -> np.ndarray:
+    """(num/den)-quantile along axis 0 with the 'higher' convention: the sorted
+    value at index ceil(num/den * (m - 1)), the index in exact integers."""
+    v = np.sort(np.asarray(v, dtype=np.float64), axis=0)
+    i = -(-(num * (v.shape[0] - 1)) // den)
+    return v[i]
+
+
+def qb_update(s: np.ndarray, b: np.ndarray, k: int) -> dict:
+    """Exact update: b_new_j = the (k/n)-quantile of r_{:,j} (its target share
+    q = m k / n of the m tokens), then centred (a common offset does not
+    change any top-k).  Returns the centred biases and the raw quantiles."""
+    r = qb_required_bias(s, b, k)
+    n = r.shape[1]
+    raw = quantile_higher(r, k, n)
+    return dict(bias=raw - raw.mean(), raw=raw, r=r)
+
+
+def qb_range(b: np.ndarray):
+    """Histogram range of the required biases: s lies in (0, 1) and every
+    cutoff is some expert's biased score, so r lies in [min b - 1, max b + 1]."""
+    b = np.asarray(b, dtype=np.float64)
+    return b.min() - 1.0, b.max() + 1.0
+
+
+def qb_histogram(s: np.ndarray, b: np.ndarray, k: int, bins: int) -> np.ndarray:
+    """n x B integer counts of the required biases r_ij in B uniform bins of
+    the range (values on the upper edge go to the last bin)."""
+    r = qb_required_bias(s, b, k)
+    lo, hi = qb_range(b)
+    w = (hi - lo) / bins
+    counts = np.zeros((r.shape[1], bins), dtype=np.int64)
+    for j in range(r.shape[1]):
+        for v in r[:, j]:
+            c = min(max(int(np.floor((v - lo) / w)), 0), bins - 1)
+            counts[j, c] += 1
+    return counts
+
+
+def qb_update_from_histogram(counts: np.ndarray, b: np.ndarray, k: int) -> dict:
+    """Quantile of each expert's histogram: the first bin whose cumulative
+    count reaches ceil(q), q = m k / n (m = the tokens counted, each expert
+    counts every token once), with linear interpolation inside that bin; then
+    centred."""
+    counts = np.asarray(counts, dtype=np.int64)
+    n, B = counts.shape
+    lo, hi = qb_range(b)
+    w = (hi - lo) / B
+    raw = np.empty(n, dtype=np.float64)
+    for j in range(n):
+        m = counts[j].sum()
+        target = int(np.ceil(m * k / n))
+        cum = 0
+        for c in range(B):
+            if counts[j, c] and cum + counts[j, c] >= target:
+                raw[j] = lo + w * (c + (target - cum) / counts[j, c])
+                break
+            cum += counts[j, c]
+        else:
+            raw[j] = hi
+    return dict(bias=raw - raw.mean(), raw=raw)
