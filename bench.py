@@ -95,9 +95,10 @@ def accounting(cfg) -> dict:
     if Fs:
         dense += 3 * Fs * d * 2 if cfg.expert_wfmt == "mxfp4" else 2 * _mat_bytes(cfg, Fs, d) + _mat_bytes(cfg, d, Fs)
     flops = 2 * E * d + (4 * l * d if l else 0) + k * 6 * F * din + 6 * Fs * d
-    # hi/lo E4M3 activation pairs with one E8M0 per 32 in, the same for h
-    act_in = 2 * din + 2 * din // 32
-    h_io = 2 * F + 2 * F // 32
+    # E4M3 activation terms (hi + lo, or one) with one E8M0 each per 32 in, the same for h
+    t = getattr(cfg, "act_terms", 2)
+    act_in = t * din + t * din // 32
+    h_io = t * F + t * F // 32
     return dict(din=din, gu_w=gu_w, dn_w=dn_w, expert=gu_w + dn_w, dense=dense, token_io=2 * d * 2,
                 flops_per_token=flops, gu_per_assign=act_in + h_io, dn_per_assign=h_io + din * 4)
 
@@ -238,6 +239,14 @@ def tensor_peaks(iters: int = 150000) -> dict:
     return {k: round(max(binding.tc_peak(k, iters) for _ in range(3)), 1) for k in binding.TC_KINDS}
 
 
+def mma_per_flop(cfg, T: int) -> int:
+    """MMA FLOPs the routed expert GEMMs execute per layer FLOP: one per
+    activation term on the split (large-batch) tiles; the interleaved
+    (small-batch) tiles always multiply a hi and a lo column."""
+    split = cfg.expert_wfmt != "mxfp4" or expert_tile(cfg, T) >= 64
+    return getattr(cfg, "act_terms", 2) if split else 2
+
+
 def rooflines(cfg, T: int, U: float, ms: float, pk: dict, tc: dict | None) -> dict:
     """The layer's roofline time for T tokens selecting U distinct experts:
     max(bytes / HBM, routed FLOPs / FP4 peak + dense FLOPs / bf16 peak), and
@@ -256,7 +265,7 @@ def rooflines(cfg, T: int, U: float, ms: float, pk: dict, tc: dict | None) -> di
         fp4 = tc["mxfp4"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
         issued = tc["e2m1_e4m3"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
         t_tensor = (f_routed / (fp4 * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
-        t_issued = (2 * f_routed / (issued * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
+        t_issued = (mma_per_flop(cfg, T) * f_routed / (issued * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
         out.update({"tensor_floor_ms": round(t_tensor, 4), "roofline_ms": round(max(t_hbm, t_tensor), 4),
                     "frac": round(max(t_hbm, t_tensor) / ms, 4),
                     "bound": "hbm" if t_hbm >= t_tensor else "tensor",
@@ -281,15 +290,17 @@ def gate_up_roofline(cfg, T: int, U: float, gu_ms: float, pk: dict, tc: dict | N
     issued = (tc or {}).get("e2m1_e4m3" if fp4 else "e4m3_e4m3")
     peak_t = issued if issued else 2.0 * pk["bf16"]
     achieved_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
-    tensor = gu_flops / gu_bytes > 1e3 * peak_t / 2 / pk["hbm"]
-    name = ("moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 hi/lo, tcgen05)" if fp4 else
+    mf = mma_per_flop(cfg, T)
+    tensor = gu_flops / gu_bytes > 1e3 * peak_t / mf / pk["hbm"]
+    terms = "hi/lo" if getattr(cfg, "act_terms", 2) == 2 else "one term (MXFP8)"
+    name = (f"moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 {terms}, tcgen05)" if fp4 else
             "moe_fp8_kernel<gate/up> (grouped E4M3 x E4M3 hi/lo, block-128 promotion, tcgen05)")
     r = {"kernel": name, "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_ms, 5)}
     if tensor:
-        ach = 2 * gu_flops / (gu_ms * 1e-3) / 1e12
+        ach = mf * gu_flops / (gu_ms * 1e-3) / 1e12
         r.update({"bound": "tensor", "achieved": round(ach, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
                   "frac": round(ach / peak_t, 4), "hbm_gbs": round(achieved_gbs, 1),
-                  "flops_note": "executed MMA FLOPs (two per layer FLOP: hi and lo activation terms)",
+                  "flops_note": f"executed MMA FLOPs ({mf} per layer FLOP: one per activation term)",
                   "peak_source": ("measured tcgen05 loop of the same MMA form" if issued else
                                   "fallback: MEASURED_PEAKS.json bf16_tflops x 2")})
     else:
@@ -386,8 +397,10 @@ def measure_config(wl, layer, xs, out, steps_min: int, warmup: int, pk: dict, tc
 
 # ------------------------------------------------------------------ ours
 # Configurations measured beside the headline one, one GPU: the token-count
-# sweep (seed 4), the Zipf-skewed prefill batch and the Kimi-K2 block.
-PER_CONFIG = (("k3_sweep", (1, 8, 32, 128, 512, 2048)), ("k3_prefill_t8192", None), ("k2_t4096", None))
+# sweep (seed 4), the Zipf-skewed prefill batch (two activation terms, and
+# one: MXFP8) and the Kimi-K2 block.
+PER_CONFIG = (("k3_sweep", (1, 8, 32, 128, 512, 2048)), ("k3_prefill_t8192", None),
+              ("k3_prefill_t8192_mxfp8", None), ("k2_t4096", None))
 
 
 def run_per_config(args, pk, tc, budget_s: float = 240.0) -> list:
@@ -507,7 +520,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("e2m1 x e4m3(hi+lo) block-scaled; bf16 dense; fp32 accumulate" if fp4 else
+        "dtype": (("e2m1 x e4m3(hi+lo) block-scaled" if cfg.act_terms == 2 else "e2m1 x e4m3 (mxfp8) block-scaled")
+                  + "; bf16 dense; fp32 accumulate" if fp4 else
                   "e4m3 x e4m3(hi+lo), fp32 block-128 scales; bf16 dense; fp32 accumulate"),
         "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to "
                 + ("MXFP4" if fp4 else "FP8 E4M3 block-128") + "; x ~ N(0,1) bf16)",

@@ -82,6 +82,12 @@ typedef struct {
   lmoe_act act;
   lmoe_wfmt expert_wfmt;
   int max_tokens;       /* largest T any call on this handle will pass */
+  int act_terms;        /* E4M3 terms per routed-expert activation (x^c into the gate/up GEMM, h into
+                           the down GEMM), each 32-value block with its own E8M0 scale: 2 (or 0, the
+                           default) = hi + lo, the second quantising the first one's residual, about
+                           16-bit precision; 1 = MXFP8, the deployment precision of the walk-through's
+                           "参数账" section (one term, half the activation bytes and MMAs at large
+                           batches; ~2-4% error per expert input).  1 needs MXFP4 experts. */
 } lmoe_config;
 
 /* Layer weights (all device pointers, borrowed).
@@ -123,8 +129,9 @@ typedef struct lmoe_ctx* lmoe_handle;
  * Errors: INVALID_ARG (null pointers, bad shapes), UNSUPPORTED (shapes the
  * kernels do not cover: d, l, F, Fs must be multiples of 32; E <= 2048;
  * k <= 32; MXFP4 experts need a latent layer, FP8 block-128 experts a
- * non-latent one without the norm and with d, F, Fs multiples of 128; the
- * current device is not an sm_103 GPU), OOM, CUDA.  On error *out is NULL. */
+ * non-latent one without the norm and with d, F, Fs multiples of 128 and
+ * two activation terms; the current device is not an sm_103 GPU), OOM,
+ * CUDA.  On error *out is NULL. */
 LMOE_API lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStream_t stream, lmoe_handle* out);
 
 /* Router only (Kimi K3 card, router steps; port notes item 3): topk_idx

@@ -38,6 +38,13 @@ __device__ __forceinline__ float glu_act_fast(float g, float u, int act, float b
   if (act == 1) return g * sg * u;
   return b1 * tanh_fast(g * (1.0f / b1)) * sg * (b2 * tanh_fast(u * (1.0f / b2)));
 }
+// h for the down pass: the fast form when h is kept as two E4M3 terms (its
+// error stays below their resolution); the accurate form when h is one E4M3
+// term, whose rounding the approximation would otherwise move for about one
+// element in a hundred.
+__device__ __forceinline__ float glu_act_terms(float g, float u, int act, float b1, float b2, int terms) {
+  return terms == 1 ? glu_act(g, u, act, b1, b2) : glu_act_fast(g, u, act, b1, b2);
+}
 
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
@@ -123,6 +130,35 @@ __device__ __forceinline__ void quant_hilo_warp_n(const float (&a)[N], HiLo (&r)
     r[u].s_lo = e4m3_block_scale(m[u]);
     r[u].q_lo = f32_to_e4m3(res[u] * e8m0_to_f32(254u - r[u].s_lo));
   }
+}
+
+// One-term form (MXFP8 activations): each value as a single E4M3 code with
+// its block's scale; the lo term is an exact zero (code 0, scale 1) so that
+// layouts holding a lo slot add nothing for it.
+template <int N>
+__device__ __forceinline__ void quant_hi_warp_n(const float (&a)[N], HiLo (&r)[N]) {
+  float m[N];
+#pragma unroll
+  for (int u = 0; u < N; ++u) m[u] = fabsf(a[u]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    r[u].s_hi = e4m3_block_scale(m[u]);
+    r[u].q_hi = f32_to_e4m3(a[u] * e8m0_to_f32(254u - r[u].s_hi));
+    r[u].q_lo = 0;
+    r[u].s_lo = 127u;
+  }
+}
+// The encoding of h for the down pass: two terms, or one (terms == 1).
+template <int N>
+__device__ __forceinline__ void quant_terms_warp_n(const float (&a)[N], HiLo (&r)[N], int terms) {
+  if (terms == 1)
+    quant_hi_warp_n<N>(a, r);
+  else
+    quant_hilo_warp_n<N>(a, r);
 }
 
 // Programmatic dependent launch: the kernels of a forward are launched with

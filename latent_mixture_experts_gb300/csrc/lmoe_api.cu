@@ -36,6 +36,7 @@ struct lmoe_ctx {
   int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
   int dx = 0;          // width the routed experts read and write: the latent, or d for non-latent layers
   bool fp8 = false;    // experts in FP8 E4M3 with 128 x 128 fp32 block scales
+  int terms = 2;       // E4M3 terms per routed-expert activation (2: hi + lo, 1: MXFP8)
   // FP8 layers run the shared expert on the FP8 expert GEMMs, as one expert
   // that every token uses (exact block-scaled weights): its tile list, identity
   // rows and unit weights, hi/lo activations and its fp32 output.
@@ -336,6 +337,8 @@ lmoe_status validate_cfg(const lmoe_config* c) {
   if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->max_tokens) * c->top_k > (1LL << 30)) return LMOE_ERR_UNSUPPORTED;
   if (c->use_latent_norm && !(c->norm_eps >= 0.f)) return LMOE_ERR_INVALID_ARG;
+  if (c->act_terms < 0 || c->act_terms > 2) return LMOE_ERR_INVALID_ARG;
+  if (c->act_terms == 1 && c->expert_wfmt != LMOE_W_MXFP4) return LMOE_ERR_UNSUPPORTED;
   return LMOE_OK;
 }
 
@@ -411,6 +414,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->Fs = cfg->d_shared_ff;
   h->dx = h->din ? h->din : h->d;
   h->fp8 = cfg->expert_wfmt == LMOE_W_FP8_BLOCK128;
+  h->terms = cfg->act_terms == 1 ? 1 : 2;
   h->Kp = static_cast<int>(align_up(h->dx, 128));
   h->Fp = static_cast<int>(align_up(h->F, 128));
   h->MT_gu = h->Fp / 128;
@@ -767,7 +771,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     StageTimer tm(h, LMOE_STAGE_SHARED, ss);
     const int BNs = fp8_tile_tokens(T, 1);
     LMOE_TRY(launch_shared_tiles(T, BNs, h->sh_tiles, h->sh_tile_off, h->sh_ntiles, ss));
-    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, h->xq_sh, h->xsf_sh, h->sched + 2, nullptr, 0, ss));
+    LMOE_TRY(launch_quant_gather_bf16(x, T, 1, d, d, h->sh_iota, BNs, 1, 2, h->xq_sh, h->xsf_sh, h->sched + 2, nullptr,
+                                      0, ss));
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.a_gate = h->m_sg;
@@ -782,6 +787,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.err = h->err;
     p.sched = h->sched + 2;
     p.KS = 1;
+    p.terms = 2;
     p.N_out = Fs;
     p.MT = Fs / kFp8Rows;
     p.KG = d / 128;
@@ -871,11 +877,11 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
     if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched,
-                                   h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
+                                   h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
     else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->xq, h->xsf, h->sched,
-                                        h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
+                                        h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
     ++launches;
     tm.done();
   }
@@ -889,7 +895,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     const int mi = RB == 256 ? 1 : 0;
     p.a_gate = h->m_exg[mi];
     p.a_up = h->m_exu[mi];
-    if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
+    // activation rows per tile: hi and lo (2 BN), or the BN hi rows of a split tile in the one-term form
+    const int b_rows = (split && h->terms == 1) ? BNm : 2 * BNm;
+    if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
+    p.terms = h->terms;
     p.sfa_gate = h->sfa_gate;
     p.sfa_up = h->sfa_up;
     p.sfb = h->xsf;
@@ -925,7 +934,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     tgu.done();
     MoeGemmParams q = p;
     q.a_gate = h->m_exd[mi];
-    if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, 2 * BNm)) return LMOE_ERR_CUDA;
+    if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
     q.sfa_gate = h->sfa_down;
     q.sfa_up = nullptr;
     q.sfb = h->hsf;

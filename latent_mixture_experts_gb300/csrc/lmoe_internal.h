@@ -97,12 +97,14 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int E, int BN, con
 //   split (split = 1): per BN-row tile b, rows 2*BN*b + j (hi) and
 //     2*BN*b + BN + j (lo), j = r - BN*b; hi and lo are two operands of
 //     N = BN columns, scale atoms [Ppad/BN][KG][2] (BN <= 128).
+// terms = 1: the hi term only (split: lo rows not written; interleaved: lo
+// rows zero with unit scales).
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                int split, int terms, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
                                 cudaStream_t s);
 // Same from bf16 token rows (layers whose experts take x itself).
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                     int split, int terms, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
                                      cudaStream_t s);
 
 // Weight rows per work item (and per TMA box) of the grouped expert GEMMs:
@@ -195,6 +197,8 @@ struct MoeGemmParams {
   int* gcnt;
   int P;
   size_t y_plane;
+  int terms;                     // activation terms: 2 (E4M3 hi + lo) or 1 (MXFP8: hi only; split
+                                 // layouts then load and multiply only the hi rows, whose TMA box is BN rows)
   int N_out;                     // output features per expert (F for gate/up, din for down)
   int MT;                        // work-item columns per expert tile: ceil(N_out / rows per item)
   int MTa;                       // 128-row tiles per (expert, k-group) in the scale-atom layout (even)

@@ -141,11 +141,11 @@ __device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t 
               gv += __ldcg(src);
               uv += __ldcg(src + plane);
             }
-            h[u] = glu_act_fast(gv, uv, p.act, p.b1, p.b2);
+            h[u] = glu_act_terms(gv, uv, p.act, p.b1, p.b2, p.terms);
           }
         }
       }
-      quant_hilo_warp_n<4>(h, e);
+      quant_terms_warp_n<4>(h, e, p.terms);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u;
@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 
   const int ntiles = *p.ntiles;
   const int KS = KSP ? p.KS : 1;
+  // one activation term on a split layout: hi rows only (interleaved layouts
+  // keep their zero lo columns)
+  const bool one = C::SPLIT && p.terms == 1;
   const int total = ntiles * p.MT * KS;
   const int KG = p.KG;
   // k-groups [g0, g1) of item w (the whole K range unless the batch is K split)
@@ -251,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             break;
           }
           const size_t sfa_off = ((sfa_row + g) * p.MTa + mt * (C::IR / 128)) * 512;
-          mbar_arrive_expect_tx(&full[s], C::kTx);
+          mbar_arrive_expect_tx(&full[s], C::kTx - (one ? C::kB / 2 + 512 : 0));
           tma_load_2d(st_a(s, 0), &p.a_gate, &full[s], g * 128, arow);
           tma_load_2d(st_a(s, 1), map1, &full[s], g * 128, arow1);
-          tma_load_2d(st_b(s), &p.b, &full[s], g * 128, 2 * row0);
+          tma_load_2d(st_b(s), &p.b, &full[s], g * 128, 2 * row0);   // one term: the BN hi rows only
           bulk_g2s(st_sfa(s, 0), p.sfa_gate + sfa_off, C::kSfa, &full[s]);
           bulk_g2s(st_sfa(s, 1), sfa1 + sfa_off, C::kSfa, &full[s]);
-          bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, C::kSfb, &full[s]);
+          bulk_g2s(st_sfb(s), p.sfb + (sfb_idx + g) * C::kSfb, one ? 512 : C::kSfb, &full[s]);
         }
         w = nxt < total ? nxt : -1;
       }
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             tmem_cp_32x128b_x4(sf + 4 * i, sdesc_noswz(smem_u32(st_sfa(s, i / C::kTiles)) + 512 * (i % C::kTiles), 16, 128));
 #pragma unroll
           for (int a = 0; a < C::NA; ++a)
-            tmem_cp_32x128b_x4(sfb + 4 * a, sdesc_noswz(smem_u32(st_sfb(s)) + 512 * a, 16, 128));
+            if (a == 0 || !one) tmem_cp_32x128b_x4(sfb + 4 * a, sdesc_noswz(smem_u32(st_sfb(s)) + 512 * a, 16, 128));
           const uint32_t bb = smem_u32(st_b(s));
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
@@ -302,8 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const uint32_t a_addr = smem_u32(st_a(s, i / C::kTiles)) + (i % C::kTiles) * 16384 + 32 * kb;
               mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + 32 * kb), idesc, sf + 4 * i, sfb, acc);
               if constexpr (C::SPLIT)   // lo rows follow the tile's BN hi rows
-                mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + BN * 128 + 32 * kb), idesc,
-                             sf + 4 * i, sfb + 4, 1u);
+                if (!one)
+                  mma_mxf8f6f4(d0 + i * C::N, sdesc_sw128(a_addr), sdesc_sw128(bb + BN * 128 + 32 * kb), idesc,
+                               sf + 4 * i, sfb + 4, 1u);
             }
           }
           mma_commit(&empty[s]);
@@ -376,19 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 HiLo e[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                  h[u] = f_ok ? glu_act_fast(__uint_as_float(rg[jq + u]), __uint_as_float(ru[jq + u]), p.act, p.b1,
-                                             p.b2)
+                  h[u] = f_ok ? glu_act_terms(__uint_as_float(rg[jq + u]), __uint_as_float(ru[jq + u]), p.act,
+                                              p.b1, p.b2, p.terms)
                               : 0.0f;
-                quant_hilo_warp_n<4>(h, e);
+                quant_terms_warp_n<4>(h, e, p.terms);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int j = j0 + jq + u;
                   if (j >= nrows) break;
                   p.hq[(hi0 + j) * p.Fp + f] = e[u].q_hi;
-                  p.hq[(hi0 + BN + j) * p.Fp + f] = e[u].q_lo;
+                  if (!one) p.hq[(hi0 + BN + j) * p.Fp + f] = e[u].q_lo;
                   if (lane == 0) {
                     atom[sf_atom_offset(j, kb)] = static_cast<uint8_t>(e[u].s_hi);
-                    atom[512 + sf_atom_offset(j, kb)] = static_cast<uint8_t>(e[u].s_lo);
+                    if (!one) atom[512 + sf_atom_offset(j, kb)] = static_cast<uint8_t>(e[u].s_lo);
                   }
                 }
               }
@@ -431,9 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 const int jj = jq + u;
                 const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
                 const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
-                h[u] = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
+                h[u] = f_ok ? glu_act_terms(gv, uv, p.act, p.b1, p.b2, p.terms) : 0.0f;
               }
-              quant_hilo_warp_n<4>(h, e);
+              quant_terms_warp_n<4>(h, e, p.terms);
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int j = j0 + jq + u;
@@ -490,7 +494,7 @@ cudaError_t launch_moe_k(const MoeGemmParams& p, int grid, cudaStream_t s) {
 // The K-split form exists for the 16-assignment tile, the one small batches use.
 template <int BN, bool GU>
 cudaError_t launch_moe(const MoeGemmParams& p, int grid, cudaStream_t s) {
-  if (!p.sched || p.KS < 1 || p.KS > p.KG) return cudaErrorInvalidValue;
+  if (!p.sched || p.KS < 1 || p.KS > p.KG || (p.terms != 1 && p.terms != 2)) return cudaErrorInvalidValue;
   if (p.KS == 1) return launch_moe_k<BN, GU, false>(p, grid, s);
   if constexpr (BN == 16) {
     if (GU && (!p.gpart || !p.gcnt)) return cudaErrorInvalidValue;
@@ -530,7 +534,7 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 
 template <typename TIn>
 __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, int din, int Kp,
-                                    const int32_t* __restrict__ inv_pad, int BN, int split,
+                                    const int32_t* __restrict__ inv_pad, int BN, int split, int terms,
                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, int* __restrict__ sched,
                                     int* __restrict__ cnt, int ncnt) {
   griddep_launch();
@@ -560,25 +564,28 @@ __global__ void quant_gather_kernel(const TIn* __restrict__ xc, int T, int k, in
     w_hi |= static_cast<uint32_t>(q) << (8 * u);
     res[u] = v[u] - e4m3_to_f32(q) * sc_hi;
   }
-  m = fmaxf(fmaxf(fabsf(res[0]), fabsf(res[1])), fmaxf(fabsf(res[2]), fabsf(res[3])));
-  const uint32_t s_lo = e4m3_block_scale(max8(m));
-  const float inv_lo = e8m0_to_f32(254u - s_lo);
-  uint32_t w_lo = 0;
+  // second term (the residual), or a zero term with a unit scale in the one-term form
+  uint32_t s_lo = 127u, w_lo = 0;
+  if (terms == 2) {
+    m = fmaxf(fmaxf(fabsf(res[0]), fabsf(res[1])), fmaxf(fabsf(res[2]), fabsf(res[3])));
+    s_lo = e4m3_block_scale(max8(m));
+    const float inv_lo = e8m0_to_f32(254u - s_lo);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) w_lo |= static_cast<uint32_t>(f32_to_e4m3(res[u] * inv_lo)) << (8 * u);
+    for (int u = 0; u < 4; ++u) w_lo |= static_cast<uint32_t>(f32_to_e4m3(res[u] * inv_lo)) << (8 * u);
+  }
 
   const int32_t* rows = inv_pad + static_cast<size_t>(t) * k;
-  if (split) {
+  if (split) {   // one term: the hi rows and hi atoms only (the GEMMs read nothing else)
     for (int j = 0; j < k; ++j) {
       const size_t row = split_row_hi(rows[j], BN);
       *reinterpret_cast<uint32_t*>(xq + row * Kp + c0) = w_hi;
-      *reinterpret_cast<uint32_t*>(xq + (row + BN) * Kp + c0) = w_lo;
+      if (terms == 2) *reinterpret_cast<uint32_t*>(xq + (row + BN) * Kp + c0) = w_lo;
     }
     for (int j = lane & 7; j < k; j += 8) {
       const int r = rows[j];
       uint8_t* at = xsf + (static_cast<size_t>(r / BN) * KG + g) * 1024 + sf_atom_offset(r % BN, kb);
       at[0] = static_cast<uint8_t>(s_hi);
-      at[512] = static_cast<uint8_t>(s_lo);
+      if (terms == 2) at[512] = static_cast<uint8_t>(s_lo);
     }
     return;
   }
@@ -814,31 +821,33 @@ cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream
 }
 
 cudaError_t launch_quant_gather(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                int split, int terms, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
                                 cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (terms != 1 && terms != 2) return cudaErrorInvalidValue;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
   {
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<float>, blocks, 32 * warps_per_block, 0, s, xc, T, k, din,
-                                      Kp, inv_pad, BN, split, xq, xsf, sched, cnt, ncnt);
+                                      Kp, inv_pad, BN, split, terms, xq, xsf, sched, cnt, ncnt);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_gather_bf16(const void* x, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
-                                     int split, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                     int split, int terms, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
                                      cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (terms != 1 && terms != 2) return cudaErrorInvalidValue;
   const int warps_per_block = 8;
   const long long warps = static_cast<long long>(T) * (Kp / 128);
   {
     const unsigned blocks = static_cast<unsigned>((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t e_ = launch_pdl(quant_gather_kernel<__nv_bfloat16>, blocks, 32 * warps_per_block, 0, s,
-                                      static_cast<const __nv_bfloat16*>(x), T, k, din, Kp, inv_pad, BN, split, xq,
-                                      xsf, sched, cnt, ncnt);
+                                      static_cast<const __nv_bfloat16*>(x), T, k, din, Kp, inv_pad, BN, split, terms,
+                                      xq, xsf, sched, cnt, ncnt);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();

@@ -33,6 +33,7 @@ class LayerConfig:
     situ_linear_beta: float = 25.0
     act: str = "situ"              # "situ" | "swiglu"
     expert_wfmt: str = "mxfp4"     # "mxfp4" | "fp8_block128"
+    act_terms: int = 2             # E4M3 terms per routed-expert activation on the GPU (1 = MXFP8)
 
     @property
     def d_expert_in(self) -> int:
@@ -78,6 +79,10 @@ WORKLOADS["k3_e64_t1024"] = Workload("k3_e64_t1024", replace(K3, n_experts=64), 
 # Kimi-K2 shapes with 32 experts (1.4 GB of FP8 expert weights) and 96
 # assignments per expert, near the 85 of the K2 T = 4096 batch.
 WORKLOADS["k2_e32_t384"] = Workload("k2_e32_t384", replace(K2, n_experts=32), T=384, seed=8)
+# The prefill batch with one E4M3 term per routed-expert activation (MXFP8,
+# the walk-through's deployment precision): same weights and tokens.
+WORKLOADS["k3_prefill_t8192_mxfp8"] = Workload("k3_prefill_t8192_mxfp8", replace(K3, act_terms=1), T=8192, seed=2,
+                                               bias="zipf")
 SWEEP_T = (1, 8, 32, 128, 512, 2048)
 for _t in SWEEP_T:
     WORKLOADS[f"k3_sweep_t{_t}"] = Workload(f"k3_sweep_t{_t}", K3, T=_t, seed=4)

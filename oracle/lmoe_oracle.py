@@ -111,6 +111,57 @@ def dequant_fp8_block128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return E4M3_VALUES[q] * scale
 
 
+# ------------------------------------------- block-scaled FP8 activations
+# The deployment precision of the routed experts' activations is MXFP8
+# (walk-through "Kimi K3 模型结构（5）", section "参数账": weights MXFP4,
+# activations MXFP8): E4M3 elements, one E8M0 scale per 32 consecutive
+# values along the contraction.  The emulation below quantises as the
+# library does, so that its one-term (MXFP8) and two-term (E4M3 hi + lo)
+# activation modes can be checked at the layer tolerance.
+E4M3_MAX = 448.0
+
+
+def e4m3_round(y: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to even, saturating at +-448:
+    3 fraction bits at binade 2^e (e >= -6), steps of 2^-9 below 2^-6."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    step = np.exp2(e - 3.0)
+    q = np.rint(a / step) * step
+    return np.sign(y) * np.minimum(q, E4M3_MAX)
+
+
+def e4m3_block_exponent(amax: np.ndarray) -> np.ndarray:
+    """p of a 32-value block's scale 2^p: the smallest power of two with
+    amax / 2^p <= 448 (no element saturates), kept to the normal range
+    [-126, 126]; p = -126 for an all-zero block."""
+    amax = np.asarray(amax, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        p = np.ceil(np.log2(amax / E4M3_MAX))
+    p = np.where(amax > 0, p, -126.0)
+    # log2 of an exact power of two times 448 can round either way: settle on the definition
+    p = np.where((amax > 0) & (amax / np.exp2(p - 1) <= E4M3_MAX), p - 1, p)
+    return np.clip(p, -126, 126)
+
+
+def mx_e4m3_terms(v: np.ndarray, terms: int) -> np.ndarray:
+    """v [..., K] (K a multiple of 32) as the sum of `terms` block-scaled E4M3
+    terms: each term quantises what the previous ones left (the first, v
+    itself) with its own per-32 scale.  Returns the represented values."""
+    v = np.asarray(v, dtype=np.float64)
+    shp = v.shape
+    blocks = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    total = np.zeros_like(blocks)
+    rest = blocks
+    for _ in range(terms):
+        p = e4m3_block_exponent(np.abs(rest).max(axis=-1))[..., None]
+        term = e4m3_round(rest / np.exp2(p)) * np.exp2(p)
+        total = total + term
+        rest = rest - term
+    return total.reshape(shp)
+
+
 # ------------------------------------------------------------ activations
 def sigmoid(z):
     with np.errstate(over="ignore"):
@@ -247,12 +298,14 @@ class Layer:
 
 
 def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
-            idx: np.ndarray | None = None) -> dict:
+            idx: np.ndarray | None = None, act_terms: int | None = None) -> dict:
     """Delta for the tokens in x (bf16 bits [T, d]).
 
     routes: a dict from `router` to reuse; idx: a given selection [T, k]
-    (its G is recomputed from this run's raw sigmoid).  Returns Delta and
-    the intermediates."""
+    (its G is recomputed from this run's raw sigmoid); act_terms: None keeps
+    the routed experts' inputs exact, 1 or 2 emulates their block-scaled
+    E4M3 encoding (x^c before the gate/up projections, h before the down
+    projection) with that many terms.  Returns Delta and the intermediates."""
     cfg = layer.cfg
     x = bf16_bits_to_f64(x_bits)
     T = x.shape[0]
@@ -267,6 +320,7 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
 
     # Latent down-projection (K3); the K2 experts take x itself.
     xe = x @ layer.dense("w_down_latent").T if cfg.d_latent else x
+    xin = mx_e4m3_terms(xe, act_terms) if act_terms else xe
 
     # moe_infer: group the assignments by expert, run each selected expert once
     # on its tokens, put the outputs back in assignment order.
@@ -278,9 +332,11 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
             continue
         assign = disp["perm"][lo:hi]
         toks = assign // k
-        g = xe[toks] @ layer.expert("ex_gate", e).T
-        u = xe[toks] @ layer.expert("ex_up", e).T
+        g = xin[toks] @ layer.expert("ex_gate", e).T
+        u = xin[toks] @ layer.expert("ex_up", e).T
         h = layer.act(g, u)
+        if act_terms:
+            h = mx_e4m3_terms(h, act_terms)
         out[assign] = h @ layer.expert("ex_down", e).T
     # Weighted sum over each token's selection (u in the pages' notation).
     u_sum = (out.reshape(T, k, -1) * G[:, :, None]).sum(axis=1)

@@ -25,7 +25,7 @@ _CFG_FIELDS = ("d_model", "d_latent", "n_experts", "top_k", "d_expert_ff", "d_sh
 def _forward_chunk(args):
     """Worker: oracle forward of one chunk of tokens with the given selection."""
     import oracle as O
-    wdir, cfgd, x_bits, idx, keep = args
+    wdir, cfgd, x_bits, idx, keep, act_terms = args
     cfg = types.SimpleNamespace(**cfgd)
     W = {}
     for f in os.listdir(wdir):
@@ -37,7 +37,7 @@ def _forward_chunk(args):
 
     W["expert_fn"] = expert_fn
     layer = O.Layer(cfg, W, cache_experts=False)
-    r = O.forward(layer, x_bits, idx=idx)
+    r = O.forward(layer, x_bits, idx=idx, act_terms=act_terms)
     return {k: r[k] for k in keep if r.get(k) is not None}
 
 
@@ -74,16 +74,18 @@ class OracleWorkers:
                 np.save(os.path.join(self.dir, f"{m}_s_{e}.npy"), self.W[m + "_s"][e].cpu().numpy())
             self.saved.add(e)
 
-    def forward(self, x_bits: np.ndarray, idx: np.ndarray, keep=("delta",)) -> dict:
+    def forward(self, x_bits: np.ndarray, idx: np.ndarray, keep=("delta",), act_terms=None) -> dict:
         """Oracle forward of tokens x_bits (bf16 bits [T, d]) with the given
-        selection idx [T, k]; returns the `keep` outputs stacked over tokens."""
+        selection idx [T, k] (act_terms: the activation emulation of
+        oracle.forward); returns the `keep` outputs stacked over tokens."""
         x_bits = np.asarray(x_bits)
         idx = np.asarray(idx)
         self._save_experts(np.unique(idx))
         T = x_bits.shape[0]
         chunks = [c for c in np.array_split(np.arange(T), min(T, 2 * self.n)) if len(c)]
         try:
-            res = self.pool.map(_forward_chunk, [(self.dir, self.cfg, x_bits[c], idx[c], keep) for c in chunks])
+            res = self.pool.map(_forward_chunk, [(self.dir, self.cfg, x_bits[c], idx[c], keep, act_terms)
+                                                 for c in chunks])
         finally:
             self._drop_experts()
         return {k: np.concatenate([r[k] for r in res]) for k in keep}

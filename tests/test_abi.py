@@ -89,6 +89,9 @@ def test_create_rejects_bad_arguments(lib):
     assert _create(lib, _cfg(n_experts=4096, top_k=2), _weights())[0] == b.LMOE_ERR_UNSUPPORTED
     assert _create(lib, _cfg(), _weights(skip=("ex_up_q",)))[0] == b.LMOE_ERR_INVALID_ARG
     assert _create(lib, _cfg(), _weights(skip=("norm_w",)))[0] == b.LMOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(act_terms=3), _weights())[0] == b.LMOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(act_terms=1, expert_wfmt=1, d_latent=0, use_latent_norm=0),
+                   _weights())[0] == b.LMOE_ERR_UNSUPPORTED     # one-term activations: MXFP4 experts only
     w = _weights()
     w.ex_gate_s = 0x10010           # 16- but not 32-byte aligned
     assert _create(lib, _cfg(), w)[0] == b.LMOE_ERR_INVALID_ARG
