@@ -234,8 +234,12 @@ LMOE_API lmoe_status lmoe_qb_update_from_histogram(lmoe_handle h, const int32_t*
  * (FP8 layers, whose shared expert runs on the FP8 expert GEMMs), "counts"
  * int32 [E], "offsets" int32 [E+1], "perm" int32 [T*k], "delta_f32" fp32
  * [T][d] (Delta before its bf16 rounding; only while lmoe_keep_f32_output
- * is on).  `bytes` must equal the tensor's size for the last T; a name the
- * layer does not have returns INVALID_ARG. */
+ * is on), "x_expert" fp32 [T*k][l] ([T*k][d] for non-latent layers) and "h"
+ * fp32 [T*k][F]: the routed experts' inputs and hidden activations per
+ * assignment a = t*k + j, as the expert GEMMs multiply them (their E4M3
+ * terms times the block scales, decoded by a kernel into dst).  `bytes`
+ * must equal the tensor's size for the last T; a name the layer does not
+ * have returns INVALID_ARG. */
 LMOE_API lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t bytes, cudaStream_t stream);
 
 /* While enabled (enable != 0), every lmoe_forward also stores Delta as fp32

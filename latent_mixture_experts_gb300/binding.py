@@ -223,6 +223,7 @@ class LatentMoE:
                   "u": ((T, dx), torch.float32), "u_hat": ((T, dx), torch.bfloat16),
                   "h_shared": ((T, c.d_shared_ff), torch.bfloat16), "y_shared": ((T, c.d_model), torch.float32),
                   "delta_f32": ((T, c.d_model), torch.float32), "counts": ((c.n_experts,), torch.int32),
+                  "x_expert": ((T * c.top_k, dx), torch.float32), "h": ((T * c.top_k, c.d_expert_ff), torch.float32),
                   "offsets": ((c.n_experts + 1,), torch.int32), "perm": ((T * c.top_k,), torch.int32)}
         shape, dt = shapes[name]
         dst = torch.empty(shape, dtype=dt, device="cuda")

@@ -26,7 +26,9 @@ __device__ __forceinline__ float glu_act(float g, float u, int act, float b1, fl
 }
 
 // Hardware approximations for the expert epilogues, whose output is encoded
-// as two E4M3 terms right after (relative error ~2^-11, below that encoding).
+// as E4M3 terms right after (relative error ~2^-11: below the resolution of
+// two terms; with one term it moves about one value in a hundred to the
+// adjacent code, a choice as valid as the rounding of the exact value).
 __device__ __forceinline__ float tanh_fast(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -37,13 +39,6 @@ __device__ __forceinline__ float glu_act_fast(float g, float u, int act, float b
   const float sg = sigmoid_fast(g);
   if (act == 1) return g * sg * u;
   return b1 * tanh_fast(g * (1.0f / b1)) * sg * (b2 * tanh_fast(u * (1.0f / b2)));
-}
-// h for the down pass: the fast form when h is kept as two E4M3 terms (its
-// error stays below their resolution); the accurate form when h is one E4M3
-// term, whose rounding the approximation would otherwise move for about one
-// element in a hundred.
-__device__ __forceinline__ float glu_act_terms(float g, float u, int act, float b1, float b2, int terms) {
-  return terms == 1 ? glu_act(g, u, act, b1, b2) : glu_act_fast(g, u, act, b1, b2);
 }
 
 __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {

@@ -94,6 +94,7 @@ struct lmoe_ctx {
   cudaEvent_t ev_fork = nullptr, ev_latent = nullptr, ev_join = nullptr;
   int last_T = 0;
   int last_launches = 0;
+  int last_BN = 0, last_split = 0;   // activation layout of the last forward's expert GEMMs
   // per-stage event timing
   bool prof = false;
   uint32_t prof_mask = 0;    // stages timed while profiling
@@ -1023,6 +1024,8 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   if (topk_w_opt) LMOE_TRY(cudaMemcpyAsync(topk_w_opt, h->G, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
   h->last_T = T;
   h->last_launches = launches;
+  h->last_BN = BNm;
+  h->last_split = split;
   return LMOE_OK;
 }
 
@@ -1064,6 +1067,15 @@ lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t
     if (!h->fp8 || !h->Fs) return LMOE_ERR_INVALID_ARG;
     src = h->y_sh;
     want = T * h->d * 4;
+  } else if (!std::strcmp(name, "x_expert") || !std::strcmp(name, "h")) {
+    // decoded in place into dst: the routed experts' inputs [T*k][dx] or hidden activations [T*k][F]
+    const bool xe = name[0] == 'x';
+    const int K = xe ? h->dx : h->F;
+    if (bytes != T * h->k * K * 4 || !h->last_BN) return LMOE_ERR_INVALID_ARG;
+    LMOE_TRY(launch_decode_terms(xe ? h->xq : h->hq, xe ? h->xsf : h->hsf, h->inv_pad, static_cast<int>(T * h->k), K,
+                                 xe ? h->Kp : h->Fp, h->last_BN, h->last_split, h->terms, static_cast<float*>(dst),
+                                 st));
+    return LMOE_OK;
   } else if (!std::strcmp(name, "delta_f32")) {
     if (!h->delta32) return LMOE_ERR_INVALID_ARG;
     src = h->delta32;

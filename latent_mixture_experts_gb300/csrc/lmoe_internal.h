@@ -251,6 +251,11 @@ cudaError_t launch_qb_from_histogram(const int32_t* counts, int E, int bins, int
 // the bounded wait then records kErrTimeout in err[0].
 cudaError_t launch_wait_timeout_probe(int* err, unsigned long long limit_ns, cudaStream_t s);
 
+// Debug read-out: the values of the encoded activations (hi + lo terms times
+// their block scales) of P assignments, fp32 [P][K], from either layout.
+cudaError_t launch_decode_terms(const uint8_t* q, const uint8_t* sf, const int32_t* inv_pad, int P, int K, int Kp,
+                                int BN, int split, int terms, float* out, cudaStream_t s);
+
 // Create-time repacking of the expert weights.
 cudaError_t launch_relayout_sfa(const uint8_t* s, int E, int N, int Kb, int MTa, int KG, uint8_t* atoms,
                                 cudaStream_t st);

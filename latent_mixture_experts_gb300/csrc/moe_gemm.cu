@@ -141,7 +141,7 @@ __device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t 
               gv += __ldcg(src);
               uv += __ldcg(src + plane);
             }
-            h[u] = glu_act_terms(gv, uv, p.act, p.b1, p.b2, p.terms);
+            h[u] = glu_act_fast(gv, uv, p.act, p.b1, p.b2);
           }
         }
       }
@@ -380,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 HiLo e[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                  h[u] = f_ok ? glu_act_terms(__uint_as_float(rg[jq + u]), __uint_as_float(ru[jq + u]), p.act,
-                                              p.b1, p.b2, p.terms)
+                  h[u] = f_ok ? glu_act_fast(__uint_as_float(rg[jq + u]), __uint_as_float(ru[jq + u]), p.act,
+                                             p.b1, p.b2)
                               : 0.0f;
                 quant_terms_warp_n<4>(h, e, p.terms);
 #pragma unroll
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 const int jj = jq + u;
                 const float gv = __uint_as_float(rg[2 * jj]) + __uint_as_float(rg[2 * jj + 1]);
                 const float uv = __uint_as_float(ru[2 * jj]) + __uint_as_float(ru[2 * jj + 1]);
-                h[u] = f_ok ? glu_act_terms(gv, uv, p.act, p.b1, p.b2, p.terms) : 0.0f;
+                h[u] = f_ok ? glu_act_fast(gv, uv, p.act, p.b1, p.b2) : 0.0f;
               }
               quant_terms_warp_n<4>(h, e, p.terms);
 #pragma unroll
@@ -799,7 +799,49 @@ int ew_grid(size_t n) {
   return static_cast<int>(g < 152 * 16 ? (g ? g : 1) : 152 * 16);
 }
 
+// Values the expert GEMMs multiply, back in fp32: for assignment a and
+// column c, the sum of its E4M3 terms (hi, and lo for two terms) times their
+// E8M0 block scales, read from either activation layout.
+__global__ void decode_terms_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                                    const int32_t* __restrict__ inv_pad, int P, int K, int Kp, int BN, int split,
+                                    int terms, float* __restrict__ out) {
+  const size_t n = static_cast<size_t>(P) * K;
+  const int KG = Kp / 128;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int a = static_cast<int>(i / K), c = static_cast<int>(i % K);
+    const int r = inv_pad[a], g = c >> 7, kb = (c & 127) >> 5;
+    uint8_t qh, ql, sh, sl;
+    if (split) {
+      const size_t row = split_row_hi(r, BN);
+      qh = q[row * Kp + c];
+      ql = q[(row + BN) * Kp + c];
+      const uint8_t* at = sf + (static_cast<size_t>(r / BN) * KG + g) * 1024 + sf_atom_offset(r % BN, kb);
+      sh = at[0];
+      sl = at[512];
+    } else {
+      qh = q[static_cast<size_t>(2 * r) * Kp + c];
+      ql = q[static_cast<size_t>(2 * r + 1) * Kp + c];
+      const int NA = (2 * BN + 127) / 128, nn = 2 * (r % BN);
+      const uint8_t* at = sf + (static_cast<size_t>(r / BN) * KG + g) * NA * 512;
+      sh = at[(nn >> 7) * 512 + sf_atom_offset(nn & 127, kb)];
+      sl = at[((nn + 1) >> 7) * 512 + sf_atom_offset((nn + 1) & 127, kb)];
+    }
+    float v = e4m3_to_f32(qh) * e8m0_to_f32(sh);
+    if (terms == 2) v += e4m3_to_f32(ql) * e8m0_to_f32(sl);
+    out[i] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_terms(const uint8_t* q, const uint8_t* sf, const int32_t* inv_pad, int P, int K, int Kp,
+                                int BN, int split, int terms, float* out, cudaStream_t s) {
+  if (P <= 0) return cudaSuccess;
+  decode_terms_kernel<<<ew_grid(static_cast<size_t>(P) * K), 256, 0, s>>>(q, sf, inv_pad, P, K, Kp, BN, split, terms,
+                                                                          out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s) {
   switch (BN) {

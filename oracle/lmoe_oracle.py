@@ -162,6 +162,30 @@ def mx_e4m3_terms(v: np.ndarray, terms: int) -> np.ndarray:
     return total.reshape(shp)
 
 
+def mx_e4m3_valid_range(v: np.ndarray, rel: float = 1e-4):
+    """The one-term encodings a computation of v can produce when it errs by
+    at most rel times its 32-value block's largest magnitude (the scale of a
+    dot product's rounding error): (lo, hi) per element, the smallest and
+    largest encoding of any value within that distance, under either block
+    scale when the block maximum itself lies that close to a scale
+    threshold.  lo == hi where the encoding is unambiguous.  Rounding a value
+    computed in lower precision is a decision taken near such boundaries, like
+    a near tie of the router; any encoding in the range is correct."""
+    v = np.asarray(v, dtype=np.float64)
+    shp = v.shape
+    blocks = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    amax = np.abs(blocks).max(axis=-1, keepdims=True)
+    d = rel * amax
+    lo, hi = None, None
+    for pa in (amax * (1 - rel), amax * (1 + rel)):
+        s = np.exp2(e4m3_block_exponent(pa))
+        a = e4m3_round((blocks - d) / s) * s
+        b = e4m3_round((blocks + d) / s) * s
+        lo = a if lo is None else np.minimum(lo, a)
+        hi = b if hi is None else np.maximum(hi, b)
+    return lo.reshape(shp), hi.reshape(shp)
+
+
 # ------------------------------------------------------------ activations
 def sigmoid(z):
     with np.errstate(over="ignore"):
@@ -298,14 +322,21 @@ class Layer:
 
 
 def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
-            idx: np.ndarray | None = None, act_terms: int | None = None) -> dict:
+            idx: np.ndarray | None = None, act_terms: int | None = None,
+            x_in: np.ndarray | None = None, h_in: np.ndarray | None = None) -> dict:
     """Delta for the tokens in x (bf16 bits [T, d]).
 
     routes: a dict from `router` to reuse; idx: a given selection [T, k]
     (its G is recomputed from this run's raw sigmoid); act_terms: None keeps
     the routed experts' inputs exact, 1 or 2 emulates their block-scaled
     E4M3 encoding (x^c before the gate/up projections, h before the down
-    projection) with that many terms.  Returns Delta and the intermediates."""
+    projection) with that many terms; x_in: the encoded expert inputs [T][dx]
+    to use instead of encoding x^c here (a choice among the encodings
+    mx_e4m3_valid_range allows, checked by the caller); h_in: likewise the
+    encoded hidden activations [T*k][F] per assignment a = t*k + j (the gate
+    and up projections are then not evaluated).  Returns Delta and the
+    intermediates (h: the hidden activations the down projections take; h_pre:
+    before their encoding)."""
     cfg = layer.cfg
     x = bf16_bits_to_f64(x_bits)
     T = x.shape[0]
@@ -320,23 +351,33 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
 
     # Latent down-projection (K3); the K2 experts take x itself.
     xe = x @ layer.dense("w_down_latent").T if cfg.d_latent else x
-    xin = mx_e4m3_terms(xe, act_terms) if act_terms else xe
+    if x_in is not None:
+        xin = np.asarray(x_in, dtype=np.float64)
+    else:
+        xin = mx_e4m3_terms(xe, act_terms) if act_terms else xe
 
     # moe_infer: group the assignments by expert, run each selected expert once
     # on its tokens, put the outputs back in assignment order.
     disp = dispatch(sel, cfg.n_experts)
     out = np.zeros((T * k, xe.shape[1]), dtype=np.float64)
+    h_all = np.zeros((T * k, cfg.d_expert_ff), dtype=np.float64)
+    h_pre = np.zeros((T * k, cfg.d_expert_ff), dtype=np.float64)
     for e in range(cfg.n_experts):
         lo, hi = disp["offsets"][e], disp["offsets"][e + 1]
         if hi == lo:
             continue
         assign = disp["perm"][lo:hi]
         toks = assign // k
-        g = xin[toks] @ layer.expert("ex_gate", e).T
-        u = xin[toks] @ layer.expert("ex_up", e).T
-        h = layer.act(g, u)
-        if act_terms:
-            h = mx_e4m3_terms(h, act_terms)
+        if h_in is not None:
+            h = np.asarray(h_in, dtype=np.float64)[assign]
+        else:
+            g = xin[toks] @ layer.expert("ex_gate", e).T
+            u = xin[toks] @ layer.expert("ex_up", e).T
+            h = layer.act(g, u)
+            h_pre[assign] = h
+            if act_terms:
+                h = mx_e4m3_terms(h, act_terms)
+        h_all[assign] = h
         out[assign] = h @ layer.expert("ex_down", e).T
     # Weighted sum over each token's selection (u in the pages' notation).
     u_sum = (out.reshape(T, k, -1) * G[:, :, None]).sum(axis=1)
@@ -357,7 +398,8 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
         h_s = None
         y_shared = np.zeros_like(y_routed)
     delta = y_routed + y_shared
-    return dict(delta=delta, routes=routes, xc=xe if cfg.d_latent else None, u=u_sum,
+    return dict(delta=delta, routes=routes, xc=xe if cfg.d_latent else None, x_in=xin, h=h_all, h_pre=h_pre,
+                u=u_sum,
                 u_hat=u_hat, y_routed=y_routed, y_shared=y_shared, h_s=h_s, dispatch=disp)
 
 

@@ -46,6 +46,68 @@ def forward_checked(layer, x):
     return (out.cpu().double().numpy(), out32.cpu().double().numpy(), idx.cpu().numpy(), Gw.cpu().numpy())
 
 
+def check_expert_io(layer, T, k, x_in, h_ref, terms, rows=None, label=""):
+    """Step-level check of the routed experts: the inputs ("x_expert") and
+    hidden activations ("h") the expert GEMMs multiplied, decoded from their
+    E4M3 terms, against the oracle's x_in [T][dx] (per token) and h
+    [T*k][F] (per assignment).  rows: the assignments to compare (default
+    all).  Two terms: within their resolution of the exact values (rel-L2 per
+    row <= 2e-3 for x, 5e-3 for h, whose g and u carry x's encoding).  One
+    term, against the oracle continuing from the GPU's validated encodings
+    (validated_one_term_inputs / _hidden): identical."""
+    xg = layer.lmoe_debug_tensor("x_expert", T).cpu().double().numpy()
+    hg = layer.lmoe_debug_tensor("h", T).cpu().double().numpy()
+    rows = np.arange(T * k) if rows is None else np.asarray(rows)
+    xw = np.asarray(x_in)[rows // k]
+    xg, hg, hw = xg[rows], hg[rows], np.asarray(h_ref)
+    rx, rh = rel_l2_per_token(xg, xw).max(), rel_l2_per_token(hg, hw).max()
+    fx, fh = (xg != xw).mean(), (hg != hw).mean()
+    print(f"{label}: expert inputs rel-L2 max {rx:.2e} ({fx:.1e} of codes differ), "
+          f"hidden rel-L2 max {rh:.2e} ({fh:.1e} differ)")
+    if terms == 1:
+        assert fx == 0 and fh == 0, (fx, fh)
+    else:
+        assert rx <= 2e-3 and rh <= 5e-3, (rx, rh)
+
+
+def validated_one_term_hidden(layer, T, h_exact, rows=None, rel=2e-3):
+    """The GPU's one-term hidden activations h [T*k][F] (rows: the
+    assignments to take), each element checked to be an encoding of a value
+    within rel x its 32-block's largest magnitude of the oracle's exact h
+    (rel = 2e-3 covers the hardware tanh and exp approximations the epilogue
+    uses, relative error ~2^-11 each).  Returns them for
+    oracle.forward(h_in=...) and the fraction that differ from the oracle's
+    own rounding."""
+    hg = layer.lmoe_debug_tensor("h", T).cpu().double().numpy()
+    if rows is not None:
+        hg = hg[np.asarray(rows)]
+    h_exact = np.asarray(h_exact, dtype=np.float64)
+    lo, hi = O.mx_e4m3_valid_range(h_exact, rel=rel)
+    ok = (lo <= hg) & (hg <= hi)
+    assert ok.all(), f"{(~ok).sum()} hidden activations outside the valid encodings"
+    return hg, (hg != O.mx_e4m3_terms(h_exact, 1)).mean()
+
+
+def validated_one_term_inputs(layer, T, k, xe_exact, rows=None):
+    """The GPU's one-term expert inputs, checked element by element to be one
+    of the encodings the oracle allows for the exact x^c (the encoding
+    itself, or at a rounding or scale boundary that an fp32 x^c can fall on
+    either side of, the other valid ones: O.mx_e4m3_valid_range).  Every
+    assignment of a token must carry the same encoding.  Returns the
+    per-token rows [len(rows)][dx] for oracle.forward(x_in=...) and the
+    fraction of elements where the GPU took another valid encoding than
+    the oracle's own rounding."""
+    xg = layer.lmoe_debug_tensor("x_expert", T).cpu().double().numpy().reshape(T, k, -1)
+    assert (xg == xg[:, :1]).all(), "assignments of one token carry different encodings"
+    xt = xg[:, 0] if rows is None else xg[np.asarray(rows), 0]
+    xe_exact = np.asarray(xe_exact, dtype=np.float64)
+    lo, hi = O.mx_e4m3_valid_range(xe_exact)
+    ok = (lo <= xt) & (xt <= hi)
+    assert ok.all(), f"{(~ok).sum()} encoded inputs outside the valid encodings"
+    other = (xt != O.mx_e4m3_terms(xe_exact, 1)).mean()
+    return xt, other
+
+
 def sample_tokens(T, n, routes, idx, seed=0):
     """Every token for T <= n; else n tokens: the first and last, up to four
     the oracle flags as near ties, one on the most loaded expert, the rest

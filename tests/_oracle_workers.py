@@ -25,7 +25,7 @@ _CFG_FIELDS = ("d_model", "d_latent", "n_experts", "top_k", "d_expert_ff", "d_sh
 def _forward_chunk(args):
     """Worker: oracle forward of one chunk of tokens with the given selection."""
     import oracle as O
-    wdir, cfgd, x_bits, idx, keep, act_terms = args
+    wdir, cfgd, x_bits, idx, keep, act_terms, x_in, h_in = args
     cfg = types.SimpleNamespace(**cfgd)
     W = {}
     for f in os.listdir(wdir):
@@ -37,7 +37,7 @@ def _forward_chunk(args):
 
     W["expert_fn"] = expert_fn
     layer = O.Layer(cfg, W, cache_experts=False)
-    r = O.forward(layer, x_bits, idx=idx, act_terms=act_terms)
+    r = O.forward(layer, x_bits, idx=idx, act_terms=act_terms, x_in=x_in, h_in=h_in)
     return {k: r[k] for k in keep if r.get(k) is not None}
 
 
@@ -74,7 +74,8 @@ class OracleWorkers:
                 np.save(os.path.join(self.dir, f"{m}_s_{e}.npy"), self.W[m + "_s"][e].cpu().numpy())
             self.saved.add(e)
 
-    def forward(self, x_bits: np.ndarray, idx: np.ndarray, keep=("delta",), act_terms=None) -> dict:
+    def forward(self, x_bits: np.ndarray, idx: np.ndarray, keep=("delta",), act_terms=None, x_in=None,
+                h_in=None) -> dict:
         """Oracle forward of tokens x_bits (bf16 bits [T, d]) with the given
         selection idx [T, k] (act_terms: the activation emulation of
         oracle.forward); returns the `keep` outputs stacked over tokens."""
@@ -84,8 +85,11 @@ class OracleWorkers:
         T = x_bits.shape[0]
         chunks = [c for c in np.array_split(np.arange(T), min(T, 2 * self.n)) if len(c)]
         try:
-            res = self.pool.map(_forward_chunk, [(self.dir, self.cfg, x_bits[c], idx[c], keep, act_terms)
-                                                 for c in chunks])
+            k = idx.shape[1]
+            res = self.pool.map(_forward_chunk, [
+                (self.dir, self.cfg, x_bits[c], idx[c], keep, act_terms, None if x_in is None else x_in[c],
+                 None if h_in is None else h_in.reshape(-1, k, h_in.shape[-1])[c].reshape(-1, h_in.shape[-1]))
+                for c in chunks])
         finally:
             self._drop_experts()
         return {k: np.concatenate([r[k] for r in res]) for k in keep}

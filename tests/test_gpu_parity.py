@@ -24,8 +24,9 @@ import torch
 import oracle as O
 from lmoe_inputs import configs as C
 from lmoe_inputs import generate as G
-from tests._harness import (assert_delta_close, forward_checked, gpu_inputs, make_layer, oracle_layer,
-                            rel_l2_per_token, sample_tokens, valid_selection, x_bits)
+from tests._harness import (assert_delta_close, check_expert_io, forward_checked, gpu_inputs, make_layer,
+                            oracle_layer, rel_l2_per_token, sample_tokens, valid_selection,
+                            validated_one_term_hidden, validated_one_term_inputs, x_bits)
 from tests._oracle_workers import OracleWorkers
 
 pytestmark = pytest.mark.gpu
@@ -278,10 +279,24 @@ def full_size_check(wl, layer, olayer, workers, x, n_sample=16, seed=0, act_term
     got, got32, idx, Gw = forward_checked(layer, x)
     r = _check_routes(wl, layer, olayer, x, idx, Gw)
     sample = sample_tokens(T, n_sample, r, idx, seed)
-    ref = workers.forward(x_bits(x)[sample], idx[sample], act_terms=act_terms)
+    x_in = h_in = None
+    other = other_h = 0.0
+    k = wl.cfg.top_k
+    rows = (np.asarray(sample)[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    if act_terms == 1:   # the oracle continues from the GPU's encodings once checked to be valid ones
+        xe = O.bf16_bits_to_f64(x_bits(x)[sample]) @ olayer.dense("w_down_latent").T   # the oracle's x^c
+        x_in, other = validated_one_term_inputs(layer, T, k, xe, rows=sample)
+        pre = workers.forward(x_bits(x)[sample], idx[sample], act_terms=1, x_in=x_in, keep=("h_pre",))
+        h_in, other_h = validated_one_term_hidden(layer, T, pre["h_pre"], rows=rows)
+    ref = workers.forward(x_bits(x)[sample], idx[sample], act_terms=act_terms, keep=("delta", "x_in", "h"),
+                          x_in=x_in, h_in=h_in)
+    xin_full = np.zeros((T, ref["x_in"].shape[1]))
+    xin_full[sample] = ref["x_in"]
+    check_expert_io(layer, T, k, xin_full, ref["h"], act_terms or 2, rows=rows, label=f"{wl.name} T={T}")
     assert_delta_close(got[sample], ref["delta"], got32[sample],
                        label=f"{wl.name} T={T} ({len(sample)} tokens, {int(r['flag'].sum())} flagged)"
-                             + (f" vs the oracle emulating {act_terms}-term activations" if act_terms else ""))
+                             + (f" vs the oracle emulating {act_terms}-term activations (other valid "
+                                f"encodings: {other:.1e} of x, {other_h:.1e} of h)" if act_terms else ""))
     return got, idx, sample
 
 

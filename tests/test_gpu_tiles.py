@@ -13,8 +13,8 @@ import torch
 
 import oracle as O
 from lmoe_inputs import configs as C
-from tests._harness import (assert_delta_close, forward_checked, gpu_inputs, make_layer, oracle_layer,
-                            rel_l2_per_token, x_bits)
+from tests._harness import (assert_delta_close, check_expert_io, forward_checked, gpu_inputs, make_layer,
+                            oracle_layer, rel_l2_per_token, x_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +37,7 @@ def test_all_token_tiles(wl, Ts):
             xt = x[:T].contiguous()
             got, got32, idx, _ = forward_checked(layer, xt)
             ref = O.forward(olayer, x_bits(xt), idx=idx)
+            check_expert_io(layer, T, wl.cfg.top_k, ref["x_in"], ref["h"], 2, label=f"{wl.name} T={T}")
             u = layer.lmoe_debug_tensor("u", T).cpu().double().numpy()
             assert rel_l2_per_token(u, ref["u"]).max() <= 1e-2, T
             assert_delta_close(got, ref["delta"], got32, label=f"{wl.name} T={T}")

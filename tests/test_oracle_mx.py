@@ -66,3 +66,22 @@ def test_layer_emulation_modes():
     r2 = rel(O.forward(L, xb, act_terms=2)["delta"])
     r1 = rel(O.forward(L, xb, act_terms=1)["delta"])
     assert r2 < 3e-3 and r1 > 1e-2, (r1, r2)
+
+
+def test_valid_range_holds_the_encoding_and_its_boundary_neighbours():
+    """The range holds the oracle's own encoding; away from boundaries it is
+    that encoding alone; a value on a rounding midpoint admits both
+    neighbours; a block maximum on a scale threshold admits both scales."""
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((8, 64))
+    lo, hi = O.mx_e4m3_valid_range(v)
+    enc = O.mx_e4m3_terms(v, 1)
+    assert np.all((lo <= enc) & (enc <= hi))
+    big = np.abs(v) > 0.1 * np.abs(v).max()
+    assert (lo[big] != hi[big]).mean() < 2e-2
+    w = np.zeros((1, 32))
+    w[0, 0] = 448.0                     # block maximum exactly on the scale threshold
+    w[0, 1] = 1.0625                    # midpoint of 1.0 and 1.125 at scale 1
+    lo, hi = O.mx_e4m3_valid_range(w)
+    assert lo[0, 1] <= 1.0 and hi[0, 1] >= 1.125
+    assert lo[0, 0] <= 448.0 <= hi[0, 0]
