@@ -97,8 +97,9 @@ def accounting(cfg) -> dict:
     flops = 2 * E * d + (4 * l * d if l else 0) + k * 6 * F * din + 6 * Fs * d
     # E4M3 activation terms (hi + lo, or one) with one E8M0 each per 32 in, the same for h
     t = getattr(cfg, "act_terms", 2)
-    act_in = t * din + t * din // 32
-    h_io = t * F + t * F // 32
+    nb = 0.5 if getattr(cfg, "act_format", "e4m3") == "e2m1" else 1.0     # bytes per code
+    act_in = int(t * din * nb) + t * din // 32
+    h_io = int(t * F * nb) + t * F // 32
     return dict(din=din, gu_w=gu_w, dn_w=dn_w, expert=gu_w + dn_w, dense=dense, token_io=2 * d * 2,
                 flops_per_token=flops, gu_per_assign=act_in + h_io, dn_per_assign=h_io + din * 4)
 
@@ -241,8 +242,11 @@ def tensor_peaks(iters: int = 150000) -> dict:
 
 def mma_per_flop(cfg, T: int) -> int:
     """MMA FLOPs the routed expert GEMMs execute per layer FLOP: one per
-    activation term on the split (large-batch) tiles; the interleaved
-    (small-batch) tiles always multiply a hi and a lo column."""
+    activation term on the split (large-batch) tiles and on the packed-FP4
+    kernel; the interleaved (small-batch) E4M3 tiles always multiply a hi and
+    a lo column."""
+    if getattr(cfg, "act_format", "e4m3") == "e2m1":
+        return getattr(cfg, "act_terms", 3)
     split = cfg.expert_wfmt != "mxfp4" or expert_tile(cfg, T) >= 64
     return getattr(cfg, "act_terms", 2) if split else 2
 
@@ -263,7 +267,8 @@ def rooflines(cfg, T: int, U: float, ms: float, pk: dict, tc: dict | None) -> di
            "hbm_frac": round(t_hbm / ms, 4), "tflops": round(T * A["flops_per_token"] / (ms * 1e-3) / 1e12, 1)}
     if tc:
         fp4 = tc["mxfp4"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
-        issued = tc["e2m1_e4m3"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"]
+        issued = (tc["mxfp4"] if getattr(cfg, "act_format", "e4m3") == "e2m1" else
+                  tc["e2m1_e4m3"] if cfg.expert_wfmt == "mxfp4" else tc["e4m3_e4m3"])
         t_tensor = (f_routed / (fp4 * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
         t_issued = (mma_per_flop(cfg, T) * f_routed / (issued * 1e12) + f_dense / (tc["bf16"] * 1e12)) * 1e3
         out.update({"tensor_floor_ms": round(t_tensor, 4), "roofline_ms": round(max(t_hbm, t_tensor), 4),
@@ -287,13 +292,16 @@ def gate_up_roofline(cfg, T: int, U: float, gu_ms: float, pk: dict, tc: dict | N
     k = cfg.top_k
     gu_bytes = U * A["gu_w"] + T * k * A["gu_per_assign"]
     gu_flops = 2.0 * T * k * 2 * cfg.d_expert_ff * A["din"]
-    issued = (tc or {}).get("e2m1_e4m3" if fp4 else "e4m3_e4m3")
+    e2m1 = getattr(cfg, "act_format", "e4m3") == "e2m1"
+    issued = (tc or {}).get("mxfp4" if e2m1 else "e2m1_e4m3" if fp4 else "e4m3_e4m3")
     peak_t = issued if issued else 2.0 * pk["bf16"]
     achieved_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
     mf = mma_per_flop(cfg, T)
     tensor = gu_flops / gu_bytes > 1e3 * peak_t / mf / pk["hbm"]
     terms = "hi/lo" if getattr(cfg, "act_terms", 2) == 2 else "one term (MXFP8)"
-    name = (f"moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 {terms}, tcgen05)" if fp4 else
+    name = (f"moe_fp4_kernel<gate/up> (grouped MXFP4 x {getattr(cfg, 'act_terms', 3)} MXFP4 terms, packed, "
+            "tcgen05 kind::mxf4)" if e2m1 else
+            f"moe_gemm_kernel<gate/up> (grouped MXFP4 x E4M3 {terms}, tcgen05)" if fp4 else
             "moe_fp8_kernel<gate/up> (grouped E4M3 x E4M3 hi/lo, block-128 promotion, tcgen05)")
     r = {"kernel": name, "bytes_per_launch": int(gu_bytes), "ms_per_launch": round(gu_ms, 5)}
     if tensor:
@@ -307,7 +315,7 @@ def gate_up_roofline(cfg, T: int, U: float, gu_ms: float, pk: dict, tc: dict | N
         r.update({"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                   "frac": round(achieved_gbs / pk["hbm"], 4),
                   "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"})
-    tr = GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
+    tr = None if e2m1 else GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
     r["traffic"] = int(tr * gu_bytes) if tr else None
     r["traffic_source"] = ("ncu dram__bytes_read+write of this kernel on a small case of the same instantiation, "
                            "scaled to this launch by its algorithmic bytes" if tr else
@@ -431,6 +439,19 @@ def run_per_config(args, pk, tc, budget_s: float = 240.0) -> list:
     return entries
 
 
+def with_activation_format(wl, args):
+    """The workload with the command line's activation format / terms, if given."""
+    over = {}
+    if getattr(args, "act_format", None):
+        over["act_format"] = args.act_format
+    if getattr(args, "act_terms", None):
+        over["act_terms"] = args.act_terms
+    if not over:
+        return wl
+    tag = "_".join(f"{k}{v}" for k, v in over.items())
+    return replace(wl, cfg=replace(wl.cfg, **over), name=f"{wl.name}_{tag}")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -450,7 +471,7 @@ def run_ours(args):
         dist.barrier()
     pk = peaks()
     tc = None if args.no_tc_peaks else tensor_peaks()
-    wl = C.workload(args.workload)
+    wl = with_activation_format(C.workload(args.workload), args)
     T, cfg = wl.T, wl.cfg
     W = G.gen_weights(wl, device="cuda")
     xs = [G.gen_x(replace(wl, seed=sd), device="cuda") for sd in replica_seeds(wl, rank)]
@@ -670,6 +691,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--no-tc-peaks", action="store_true", help="skip the tensor-pipe peak measurement")
+    ap.add_argument("--act-format", choices=["e4m3", "e2m1"], default=None,
+                    help="routed-expert activation format (default: the workload's)")
+    ap.add_argument("--act-terms", type=int, default=None, help="activation terms (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

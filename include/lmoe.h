@@ -61,6 +61,12 @@ typedef enum {
 } lmoe_status;
 
 typedef enum { LMOE_ACT_SITU = 0, LMOE_ACT_SWIGLU = 1 } lmoe_act;
+/* Number format of the routed experts' activations on the tensor cores. */
+typedef enum {
+  LMOE_ACT_FMT_E4M3 = 0, /* E4M3 terms x the weights' own codes, kind::mxf8f6f4 (act_terms 1 or 2) */
+  LMOE_ACT_FMT_E2M1 = 1  /* packed E2M1 terms, E8M0 per 32, x MXFP4 weights as stored, both operands 4-bit in
+                            shared memory, kind::mxf4 (act_terms 1..4, 0 = 3); MXFP4 experts only */
+} lmoe_act_fmt;
 typedef enum { LMOE_W_MXFP4 = 0, LMOE_W_FP8_BLOCK128 = 1 } lmoe_wfmt;
 
 /* Layer shape and constants; keys mirror the model config (num_experts,
@@ -87,7 +93,9 @@ typedef struct {
                            default) = hi + lo, the second quantising the first one's residual, about
                            16-bit precision; 1 = MXFP8, the deployment precision of the walk-through's
                            "参数账" section (one term, half the activation bytes and MMAs at large
-                           batches; ~2-4% error per expert input).  1 needs MXFP4 experts. */
+                           batches; ~2-4% error per expert input).  1 needs MXFP4 experts.  With
+                           act_format LMOE_ACT_FMT_E2M1: MXFP4 terms, 1..4 (0 = 3). */
+  lmoe_act_fmt act_format;
 } lmoe_config;
 
 /* Layer weights (all device pointers, borrowed).

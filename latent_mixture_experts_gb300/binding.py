@@ -38,7 +38,8 @@ class LmoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int), ("d_expert_ff", ctypes.c_int), ("d_shared_ff", ctypes.c_int),
                 ("use_latent_norm", ctypes.c_int), ("norm_eps", ctypes.c_float), ("routed_scale", ctypes.c_float),
                 ("situ_beta", ctypes.c_float), ("situ_linear_beta", ctypes.c_float), ("act", ctypes.c_int),
-                ("expert_wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int), ("act_terms", ctypes.c_int)]
+                ("expert_wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int), ("act_terms", ctypes.c_int),
+                ("act_format", ctypes.c_int)]
 
 
 _WEIGHT_FIELDS = ("router_w", "router_bias", "w_down_latent", "w_up_latent", "norm_w", "ex_gate_q", "ex_up_q",
@@ -151,7 +152,8 @@ def make_config(cfg, max_tokens: int) -> LmoeConfig:
                       situ_linear_beta=cfg.situ_linear_beta,
                       act=LMOE_ACT_SITU if cfg.act == "situ" else LMOE_ACT_SWIGLU,
                       expert_wfmt=LMOE_W_MXFP4 if cfg.expert_wfmt == "mxfp4" else LMOE_W_FP8_BLOCK128,
-                      max_tokens=int(max_tokens), act_terms=int(getattr(cfg, "act_terms", 2)))
+                      max_tokens=int(max_tokens), act_terms=int(getattr(cfg, "act_terms", 2)),
+                      act_format=1 if getattr(cfg, "act_format", "e4m3") == "e2m1" else 0)
 
 
 class LatentMoE:

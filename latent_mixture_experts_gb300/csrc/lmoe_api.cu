@@ -36,7 +36,8 @@ struct lmoe_ctx {
   int d = 0, din = 0, E = 0, k = 0, F = 0, Fs = 0;
   int dx = 0;          // width the routed experts read and write: the latent, or d for non-latent layers
   bool fp8 = false;    // experts in FP8 E4M3 with 128 x 128 fp32 block scales
-  int terms = 2;       // E4M3 terms per routed-expert activation (2: hi + lo, 1: MXFP8)
+  int terms = 2;       // activation terms per routed-expert input (E4M3: 2 hi + lo, 1 MXFP8; E2M1: 1..4)
+  bool fp4 = false;    // packed E2M1 activations x MXFP4 weights (kind::mxf4nvf4); K padded to 256
   // FP8 layers run the shared expert on the FP8 expert GEMMs, as one expert
   // that every token uses (exact block-scaled weights): its tile list, identity
   // rows and unit weights, hi/lo activations and its fp32 output.
@@ -143,7 +144,7 @@ int expert_ksplit(const lmoe_ctx* h, long long P, bool gate_up) {
   if (BN != 16) return 1;   // the K-split form is built for the 16-assignment tile
   const int RB = moe_rows_per_item(BN);
   const long long MT = gate_up ? ceil_div(h->F, RB) : ceil_div(h->dx, 2 * RB);
-  const int KG = gate_up ? h->KG_gu : h->KG_dn;
+  const int KG = (gate_up ? h->KG_gu : h->KG_dn) / (h->fp4 ? 2 : 1);   // K groups of the kernel that runs
   const long long tiles = std::min<long long>(P, P / BN + std::min<long long>(h->E, P));
   const long long items = tiles * MT;
   if (items >= 2LL * h->num_sms) return 1;
@@ -338,8 +339,10 @@ lmoe_status validate_cfg(const lmoe_config* c) {
   if (c->n_experts > kMaxExperts || c->top_k > 32) return LMOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->max_tokens) * c->top_k > (1LL << 30)) return LMOE_ERR_UNSUPPORTED;
   if (c->use_latent_norm && !(c->norm_eps >= 0.f)) return LMOE_ERR_INVALID_ARG;
-  if (c->act_terms < 0 || c->act_terms > 2) return LMOE_ERR_INVALID_ARG;
+  if (c->act_format != LMOE_ACT_FMT_E4M3 && c->act_format != LMOE_ACT_FMT_E2M1) return LMOE_ERR_INVALID_ARG;
+  if (c->act_terms < 0 || c->act_terms > (c->act_format == LMOE_ACT_FMT_E2M1 ? 4 : 2)) return LMOE_ERR_INVALID_ARG;
   if (c->act_terms == 1 && c->expert_wfmt != LMOE_W_MXFP4) return LMOE_ERR_UNSUPPORTED;
+  if (c->act_format == LMOE_ACT_FMT_E2M1 && c->expert_wfmt != LMOE_W_MXFP4) return LMOE_ERR_UNSUPPORTED;
   return LMOE_OK;
 }
 
@@ -415,9 +418,11 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->Fs = cfg->d_shared_ff;
   h->dx = h->din ? h->din : h->d;
   h->fp8 = cfg->expert_wfmt == LMOE_W_FP8_BLOCK128;
-  h->terms = cfg->act_terms == 1 ? 1 : 2;
-  h->Kp = static_cast<int>(align_up(h->dx, 128));
-  h->Fp = static_cast<int>(align_up(h->F, 128));
+  h->fp4 = cfg->act_format == LMOE_ACT_FMT_E2M1;
+  h->terms = h->fp4 ? (cfg->act_terms ? cfg->act_terms : 3) : (cfg->act_terms == 1 ? 1 : 2);
+  // contraction lengths of the expert GEMMs, padded to their K group (256 for packed 4-bit rows)
+  h->Kp = static_cast<int>(align_up(h->dx, h->fp4 ? 256 : 128));
+  h->Fp = static_cast<int>(align_up(h->F, h->fp4 ? 256 : 128));
   h->MT_gu = h->Fp / 128;
   h->MT_dn = ceil_div(h->dx, 128);
   h->MTa_gu = (h->MT_gu + 1) / 2 * 2;
@@ -449,8 +454,10 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
                   2LL * h->Fs
             : 0LL,
       h->din ? max_split_rows(ceil_div(h->din, 128), 0, ceil_div(h->d, 64), h->Tm, h->num_sms, true) * h->din : 0LL);
-  const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * 2 * 512;
-  const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * 2 * 512;
+  // activation scale atoms per 16-row tile and 128 K: two E4M3 terms, or up to four E2M1 terms
+  const int atoms_per = h->fp4 ? 4 : 2;
+  const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * atoms_per * 512;
+  const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * atoms_per * 512;
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
   const size_t sfa_gu_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512;
   const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512;
@@ -608,6 +615,10 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
       ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
       ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
       ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->dx, rows);
+    } else if (h->fp4) {   // packed codes as bytes: a 128-byte box row is 256 K values
+      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp / 2, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp / 2, static_cast<long long>(h->E) * h->F, rows);
+      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp / 2, static_cast<long long>(h->E) * h->dx, rows);
     } else {
       ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
       ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
@@ -877,7 +888,10 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   // 5 activations -> hi/lo E4M3 in expert-tile order
   {
     StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
-    if (din)
+    if (h->fp4)
+      LMOE_TRY(launch_quant_gather_fp4(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->terms, h->xq, h->xsf, h->sched,
+                                       h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+    else if (din)
       LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
                                    h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
     else
@@ -896,9 +910,14 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     const int mi = RB == 256 ? 1 : 0;
     p.a_gate = h->m_exg[mi];
     p.a_up = h->m_exu[mi];
-    // activation rows per tile: hi and lo (2 BN), or the BN hi rows of a split tile in the one-term form
-    const int b_rows = (split && h->terms == 1) ? BNm : 2 * BNm;
-    if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
+    // activation rows per tile: hi and lo (2 BN), or the BN hi rows of a split tile in the one-term form;
+    // packed 4-bit terms: one box of BN rows per term
+    const int b_rows = h->fp4 ? BNm : (split && h->terms == 1) ? BNm : 2 * BNm;
+    if (h->fp4) {
+      if (!map_u8(&p.b, h->xq, h->Kp / 2, static_cast<long long>(h->terms) * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
+    } else if (!map_u8(&p.b, h->xq, h->Kp, 2LL * h->Ppad, b_rows)) {
+      return LMOE_ERR_CUDA;
+    }
     p.terms = h->terms;
     p.sfa_gate = h->sfa_gate;
     p.sfa_up = h->sfa_up;
@@ -917,7 +936,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.N_out = h->F;
     p.MT = ceil_div(h->F, RB);
     p.MTa = h->MTa_gu;
-    p.KG = h->KG_gu;
+    p.KG = h->fp4 ? h->Kp / 256 : h->KG_gu;
     p.hq = h->hq;
     p.hsf = h->hsf;
     p.Fp = h->Fp;
@@ -930,12 +949,18 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.NB = ceil_div(h->F, 128);
     p.KB = ceil_div(dx, 128);
     StageTimer tgu(h, LMOE_STAGE_EXPERT_GU, st);
-    LMOE_TRY(h->fp8 ? launch_moe_fp8_gate_up(p, BNm, h->num_sms, st) : launch_moe_gate_up(p, BNm, h->num_sms, st));
+    LMOE_TRY(h->fp8   ? launch_moe_fp8_gate_up(p, BNm, h->num_sms, st)
+             : h->fp4 ? launch_moe_fp4_gate_up(p, BNm, h->num_sms, st)
+                      : launch_moe_gate_up(p, BNm, h->num_sms, st));
     ++launches;
     tgu.done();
     MoeGemmParams q = p;
     q.a_gate = h->m_exd[mi];
-    if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
+    if (h->fp4) {
+      if (!map_u8(&q.b, h->hq, h->Fp / 2, static_cast<long long>(h->terms) * h->Ppad, b_rows)) return LMOE_ERR_CUDA;
+    } else if (!map_u8(&q.b, h->hq, h->Fp, 2LL * h->Ppad, b_rows)) {
+      return LMOE_ERR_CUDA;
+    }
     q.sfa_gate = h->sfa_down;
     q.sfa_up = nullptr;
     q.sfb = h->hsf;
@@ -945,13 +970,15 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     q.N_out = dx;
     q.MT = ceil_div(dx, 2 * RB);
     q.MTa = h->MTa_dn;
-    q.KG = h->KG_dn;
+    q.KG = h->fp4 ? h->Fp / 256 : h->KG_dn;
     q.wsc0 = static_cast<const float*>(h->w.ex_down_s);
     q.wsc1 = nullptr;
     q.NB = ceil_div(dx, 128);
     q.KB = ceil_div(h->F, 128);
     StageTimer tdn(h, LMOE_STAGE_EXPERT_DOWN, st);
-    LMOE_TRY(h->fp8 ? launch_moe_fp8_down(q, BNm, h->num_sms, st) : launch_moe_down(q, BNm, h->num_sms, st));
+    LMOE_TRY(h->fp8   ? launch_moe_fp8_down(q, BNm, h->num_sms, st)
+             : h->fp4 ? launch_moe_fp4_down(q, BNm, h->num_sms, st)
+                      : launch_moe_down(q, BNm, h->num_sms, st));
     ++launches;
     tdn.done();
   }
@@ -1072,9 +1099,13 @@ lmoe_status lmoe_debug_tensor(lmoe_handle h, const char* name, void* dst, size_t
     const bool xe = name[0] == 'x';
     const int K = xe ? h->dx : h->F;
     if (bytes != T * h->k * K * 4 || !h->last_BN) return LMOE_ERR_INVALID_ARG;
-    LMOE_TRY(launch_decode_terms(xe ? h->xq : h->hq, xe ? h->xsf : h->hsf, h->inv_pad, static_cast<int>(T * h->k), K,
-                                 xe ? h->Kp : h->Fp, h->last_BN, h->last_split, h->terms, static_cast<float*>(dst),
-                                 st));
+    if (h->fp4)
+      LMOE_TRY(launch_decode_fp4(xe ? h->xq : h->hq, xe ? h->xsf : h->hsf, h->inv_pad, static_cast<int>(T * h->k), K,
+                                 xe ? h->Kp : h->Fp, h->last_BN, h->terms, static_cast<float*>(dst), st));
+    else
+      LMOE_TRY(launch_decode_terms(xe ? h->xq : h->hq, xe ? h->xsf : h->hsf, h->inv_pad, static_cast<int>(T * h->k), K,
+                                   xe ? h->Kp : h->Fp, h->last_BN, h->last_split, h->terms, static_cast<float*>(dst),
+                                   st));
     return LMOE_OK;
   } else if (!std::strcmp(name, "delta_f32")) {
     if (!h->delta32) return LMOE_ERR_INVALID_ARG;

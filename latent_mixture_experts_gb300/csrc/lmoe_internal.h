@@ -197,6 +197,7 @@ struct MoeGemmParams {
   int* gcnt;
   int P;
   size_t y_plane;
+  int stages, accbufs;           // packed-FP4 kernel: stage ring depth and accumulator buffers (set at launch)
   int terms;                     // activation terms: 2 (E4M3 hi + lo) or 1 (MXFP8: hi only; split
                                  // layouts then load and multiply only the hi rows, whose TMA box is BN rows)
   int N_out;                     // output features per expert (F for gate/up, din for down)
@@ -250,6 +251,20 @@ cudaError_t launch_qb_from_histogram(const int32_t* counts, int E, int bins, int
 // One warp waits on an mbarrier nothing arrives at, with the given limit;
 // the bounded wait then records kErrTimeout in err[0].
 cudaError_t launch_wait_timeout_probe(int* err, unsigned long long limit_ns, cudaStream_t s);
+
+// Routed experts with packed E2M1 operands on both sides (kind::mxf4,
+// E8M0 scales per 32): weights as stored, activations p.terms MXFP4 terms in
+// the packed layout below; p.KG counts 256-K groups (K padded to 256), the
+// scale atoms are those of the other expert kernels (per 128 K).
+cudaError_t launch_moe_fp4_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+cudaError_t launch_moe_fp4_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
+// x^c rows -> `terms` MXFP4 terms per value: packed codes [Ppad/BN][terms][BN][Kp/2] (per tile, its
+// terms' rows one after the other), scale atoms [Ppad/BN][Kp/128][terms][512].
+cudaError_t launch_quant_gather_fp4(const float* xc, int T, int k, int din, int Kp, const int32_t* inv_pad, int BN,
+                                    int terms, uint8_t* xq, uint8_t* xsf, int* sched, int* cnt, int ncnt,
+                                    cudaStream_t s);
+cudaError_t launch_decode_fp4(const uint8_t* q, const uint8_t* sf, const int32_t* inv_pad, int P, int K, int Kp,
+                              int BN, int terms, float* out, cudaStream_t s);
 
 // Debug read-out: the values of the encoded activations (hi + lo terms times
 // their block scales) of P assignments, fp32 [P][K], from either layout.

@@ -33,7 +33,8 @@ class LayerConfig:
     situ_linear_beta: float = 25.0
     act: str = "situ"              # "situ" | "swiglu"
     expert_wfmt: str = "mxfp4"     # "mxfp4" | "fp8_block128"
-    act_terms: int = 2             # E4M3 terms per routed-expert activation on the GPU (1 = MXFP8)
+    act_terms: int = 2             # activation terms per routed-expert input on the GPU (E4M3: 1 = MXFP8)
+    act_format: str = "e4m3"       # "e4m3" (E4M3 terms) | "e2m1" (packed MXFP4 terms, 4-bit x 4-bit MMAs)
 
     @property
     def d_expert_in(self) -> int:

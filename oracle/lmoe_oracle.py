@@ -162,6 +162,56 @@ def mx_e4m3_terms(v: np.ndarray, terms: int) -> np.ndarray:
     return total.reshape(shp)
 
 
+E2M1_MAX = 6.0
+
+
+def e2m1_round(y: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+    negatives), ties to the even code, saturating at +-6."""
+    y = np.asarray(y, dtype=np.float64)
+    grid = E2M1_VALUES[:8]                                   # codes 0..7, ascending magnitudes
+    a = np.minimum(np.abs(y), E2M1_MAX)[..., None]
+    dist = np.abs(a - grid)
+    best = dist.min(axis=-1, keepdims=True)
+    cand = dist == best                                      # one code, or two at a midpoint
+    even = cand & (np.arange(8) % 2 == 0)
+    code = np.where(even.any(-1), np.argmax(even, -1), np.argmax(cand, -1))
+    return np.sign(y) * grid[code]
+
+
+def e2m1_block_exponent(amax: np.ndarray) -> np.ndarray:
+    """p of a 32-value block's scale 2^p for E2M1 terms: the smallest power of
+    two with amax / 2^p <= 6 (no element saturates), within [-126, 126];
+    p = -126 for an all-zero block."""
+    amax = np.asarray(amax, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        p = np.ceil(np.log2(amax / E2M1_MAX))
+    p = np.where(amax > 0, p, -126.0)
+    p = np.where((amax > 0) & (amax / np.exp2(p - 1) <= E2M1_MAX), p - 1, p)
+    return np.clip(p, -126, 126)
+
+
+def mx_e2m1_terms(v: np.ndarray, terms: int) -> np.ndarray:
+    """v [..., K] (K a multiple of 32) as the sum of `terms` MXFP4 terms, each
+    quantising what the previous ones left with its own E8M0 scale per 32."""
+    v = np.asarray(v, dtype=np.float64)
+    shp = v.shape
+    blocks = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    total = np.zeros_like(blocks)
+    rest = blocks
+    for _ in range(terms):
+        p = e2m1_block_exponent(np.abs(rest).max(axis=-1))[..., None]
+        term = e2m1_round(rest / np.exp2(p)) * np.exp2(p)
+        total = total + term
+        rest = rest - term
+    return total.reshape(shp)
+
+
+def act_encode(v: np.ndarray, terms: int, fmt: str = "e4m3") -> np.ndarray:
+    """The block-scaled encoding of the routed experts' inputs: E4M3 or E2M1 terms."""
+    return mx_e2m1_terms(v, terms) if fmt == "e2m1" else mx_e4m3_terms(v, terms)
+
+
 def mx_e4m3_valid_range(v: np.ndarray, rel: float = 1e-4):
     """The one-term encodings a computation of v can produce when it errs by
     at most rel times its 32-value block's largest magnitude (the scale of a
@@ -323,14 +373,15 @@ class Layer:
 
 def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
             idx: np.ndarray | None = None, act_terms: int | None = None,
-            x_in: np.ndarray | None = None, h_in: np.ndarray | None = None) -> dict:
+            x_in: np.ndarray | None = None, h_in: np.ndarray | None = None, act_format: str = "e4m3") -> dict:
     """Delta for the tokens in x (bf16 bits [T, d]).
 
     routes: a dict from `router` to reuse; idx: a given selection [T, k]
     (its G is recomputed from this run's raw sigmoid); act_terms: None keeps
     the routed experts' inputs exact, 1 or 2 emulates their block-scaled
-    E4M3 encoding (x^c before the gate/up projections, h before the down
-    projection) with that many terms; x_in: the encoded expert inputs [T][dx]
+    E4M3 (act_format "e4m3") or E2M1 ("e2m1") encoding (x^c before the
+    gate/up projections, h before the down projection) with that many terms;
+    x_in: the encoded expert inputs [T][dx]
     to use instead of encoding x^c here (a choice among the encodings
     mx_e4m3_valid_range allows, checked by the caller); h_in: likewise the
     encoded hidden activations [T*k][F] per assignment a = t*k + j (the gate
@@ -354,7 +405,7 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
     if x_in is not None:
         xin = np.asarray(x_in, dtype=np.float64)
     else:
-        xin = mx_e4m3_terms(xe, act_terms) if act_terms else xe
+        xin = act_encode(xe, act_terms, act_format) if act_terms else xe
 
     # moe_infer: group the assignments by expert, run each selected expert once
     # on its tokens, put the outputs back in assignment order.
@@ -376,7 +427,7 @@ def forward(layer: Layer, x_bits: np.ndarray, routes: dict | None = None,
             h = layer.act(g, u)
             h_pre[assign] = h
             if act_terms:
-                h = mx_e4m3_terms(h, act_terms)
+                h = act_encode(h, act_terms, act_format)
         h_all[assign] = h
         out[assign] = h @ layer.expert("ex_down", e).T
     # Weighted sum over each token's selection (u in the pages' notation).

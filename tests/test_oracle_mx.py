@@ -85,3 +85,31 @@ def test_valid_range_holds_the_encoding_and_its_boundary_neighbours():
     lo, hi = O.mx_e4m3_valid_range(w)
     assert lo[0, 1] <= 1.0 and hi[0, 1] >= 1.125
     assert lo[0, 0] <= 448.0 <= hi[0, 0]
+
+
+def test_e2m1_rounding_is_nearest_with_ties_to_even_codes():
+    """Against the grid the format defines (pinned code by code elsewhere):
+    every result is a nearest grid point; at midpoints, the even code."""
+    grid = O.E2M1_VALUES[:8]
+    rng = np.random.default_rng(4)
+    v = rng.uniform(-7, 7, 100000)
+    r = O.e2m1_round(v)
+    d = np.abs(np.minimum(np.abs(v), 6.0)[:, None] - grid[None, :]).min(1)
+    assert np.allclose(np.abs(np.minimum(np.abs(v), 6.0) - np.abs(r)), d, rtol=0, atol=1e-15)
+    mids = (grid[:-1] + grid[1:]) / 2                      # 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5
+    assert list(O.e2m1_round(mids)) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+    assert O.e2m1_round(np.array([-9.0]))[0] == -6.0
+
+
+def test_e2m1_terms_converge():
+    """Each MXFP4 term shrinks the residual: three terms reach ~1e-3 relative
+    error per GEMM input (two E4M3 terms' precision), four a few 1e-4; the
+    block exponent is the smallest non-saturating one."""
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((32, 3584)) * np.exp(rng.standard_normal((32, 1)))
+    errs = [np.linalg.norm(O.mx_e2m1_terms(v, t) - v) / np.linalg.norm(v) for t in (1, 2, 3, 4)]
+    assert errs[0] > errs[1] > errs[2] > errs[3]
+    assert 3e-4 < errs[2] < 5e-3 and errs[3] < 1e-3
+    a = np.abs(rng.standard_normal(5000)) * 10.0 ** rng.uniform(-20, 20, 5000)
+    for x, p in zip(a, O.e2m1_block_exponent(a)):
+        assert p == next(q for q in range(-126, 127) if x / 2.0 ** q <= 6.0)
