@@ -96,6 +96,12 @@ typedef struct {
                            batches; ~2-4% error per expert input).  1 needs MXFP4 experts.  With
                            act_format LMOE_ACT_FMT_E2M1: MXFP4 terms, 1..4 (0 = 3). */
   lmoe_act_fmt act_format;
+  int ep_size;          /* expert parallelism over ep_size ranks (0 or 1: none); the experts are split
+                           into contiguous ranges of n_experts / ep_size, and this handle's weights
+                           hold only its own range (ex_* arrays of n_experts / ep_size experts) */
+  int ep_rank;          /* this handle's rank, 0 <= ep_rank < ep_size */
+  int max_recv_rows;    /* largest number of rows lmoe_ep_experts will receive
+                           (0: ep_size * max_tokens * top_k) */
 } lmoe_config;
 
 /* Layer weights (all device pointers, borrowed).
@@ -153,6 +159,43 @@ LMOE_API lmoe_status lmoe_route(lmoe_handle h, const void* x_bf16, int T, int32_
  * NULL, receive the routing of lmoe_route.  T = 0 is a no-op. */
 LMOE_API lmoe_status lmoe_forward(lmoe_handle h, const void* x_bf16, int T, void* out_bf16, int32_t* topk_idx_opt,
                          float* topk_w_opt, cudaStream_t stream);
+
+/* Expert parallelism (Kimi K2 card, moe_infer under ep_size > 1: count
+ * exchange, token all-to-all, local regrouping, experts, reverse all-to-all,
+ * weighted sum), at the latent width for latent layers (walk-through: both
+ * passes then move 3584-wide rows).  The exchanges are the caller's (one
+ * process per GPU; an all-to-all of its collective library); the three calls
+ * below are the device work between them, stream-ordered, each on the same
+ * handle and stream in this order.  A handle with ep_size > 1 rejects
+ * lmoe_forward (UNSUPPORTED); with ep_size <= 1 these calls run all experts
+ * locally (the exchanges then pass the buffers through unchanged).
+ *
+ * lmoe_ep_dispatch: router, top-k and the grouping of the T*k assignments by
+ * global expert, plus the side-stream steps (latent down-projection, shared
+ * expert).  send_bf16 [T*k][l] (d for non-latent layers) receives each
+ * assignment's expert input in bf16, rows grouped by expert, so the rows for
+ * rank r are the contiguous block of experts [r E/R, (r+1) E/R); its row
+ * count is the sum of expert_counts over that range.  expert_counts int32
+ * [E] device.  topk_idx_opt / topk_w_opt as in lmoe_forward. */
+LMOE_API lmoe_status lmoe_ep_dispatch(lmoe_handle h, const void* x_bf16, int T, void* send_bf16,
+                                      int32_t* expert_counts, int32_t* topk_idx_opt, float* topk_w_opt,
+                                      cudaStream_t stream);
+/* lmoe_ep_experts: the rows this rank received (recv_bf16 [n][l], in the
+ * order the exchange delivers them: source rank by source rank, each
+ * source's rows grouped by this rank's experts) and recv_counts int32
+ * [ep_size][E/ep_size] (device: the rows each source sent to each local
+ * expert, the counts exchange's output) -> out_bf16 [n][l], each row's
+ * expert output (unweighted) in the same order, ready for the reverse
+ * exchange.  n <= max_recv_rows.  Counts that do not sum to n are reported
+ * by lmoe_sync_status (INVALID_ARG). */
+LMOE_API lmoe_status lmoe_ep_experts(lmoe_handle h, const void* recv_bf16, const int32_t* recv_counts, int n,
+                                     void* out_bf16, cudaStream_t stream);
+/* lmoe_ep_combine: ret_bf16 [T*k][l] = the expert outputs returned in the
+ * order of lmoe_ep_dispatch's send rows; weights them by G, sums each
+ * token's k slots in slot order, applies the latent RMSNorm and the output
+ * GEMM with the shared expert: out_bf16 [T][d] = Delta.  T must be the last
+ * lmoe_ep_dispatch's. */
+LMOE_API lmoe_status lmoe_ep_combine(lmoe_handle h, const void* ret_bf16, int T, void* out_bf16, cudaStream_t stream);
 
 /* lmoe_forward on HOST buffers: copies x (bf16 [T][d], host memory; pinned
  * for asynchronous copies) into the workspace, runs the layer and copies

@@ -25,7 +25,8 @@ EXPORTS = ("lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_forward_host", "lm
            "lmoe_set_profiling_period",
            "lmoe_profile_get", "lmoe_last_active_experts", "lmoe_destroy", "lmoe_status_string",
            "lmoe_dispatch_noalloc", "lmoe_keep_f32_output", "lmoe_selftest_timeout", "lmoe_tc_peak",
-           "lmoe_qb_update", "lmoe_qb_histogram", "lmoe_qb_update_from_histogram")
+           "lmoe_qb_update", "lmoe_qb_histogram", "lmoe_qb_update_from_histogram",
+           "lmoe_ep_dispatch", "lmoe_ep_experts", "lmoe_ep_combine")
 NOALLOC_MAX_ASSIGNMENTS = 65536
 NOALLOC_MAX_EXPERTS = 2048
 PROFILE_ALL_STAGES = 0x1FF
@@ -39,7 +40,8 @@ class LmoeConfig(ctypes.Structure):
                 ("use_latent_norm", ctypes.c_int), ("norm_eps", ctypes.c_float), ("routed_scale", ctypes.c_float),
                 ("situ_beta", ctypes.c_float), ("situ_linear_beta", ctypes.c_float), ("act", ctypes.c_int),
                 ("expert_wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int), ("act_terms", ctypes.c_int),
-                ("act_format", ctypes.c_int)]
+                ("act_format", ctypes.c_int), ("ep_size", ctypes.c_int), ("ep_rank", ctypes.c_int),
+                ("max_recv_rows", ctypes.c_int)]
 
 
 _WEIGHT_FIELDS = ("router_w", "router_bias", "w_down_latent", "w_up_latent", "norm_w", "ex_gate_q", "ex_up_q",
@@ -92,6 +94,9 @@ def load_library(path: str = LIB_PATH):
             "lmoe_qb_update": (I, [P, P, I, P, P, P]),
             "lmoe_qb_histogram": (I, [P, P, I, P, I, P, P]),
             "lmoe_qb_update_from_histogram": (I, [P, P, I, P, P, P]),
+            "lmoe_ep_dispatch": (I, [P, P, I, P, P, P, P, P]),
+            "lmoe_ep_experts": (I, [P, P, P, I, P, P]),
+            "lmoe_ep_combine": (I, [P, P, I, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -143,7 +148,7 @@ def tc_peak(kind: str, iters: int, stream=None) -> float:
     return fl.value / (ms.value * 1e-3) / 1e12
 
 
-def make_config(cfg, max_tokens: int) -> LmoeConfig:
+def make_config(cfg, max_tokens: int, ep_size: int = 1, ep_rank: int = 0, max_recv_rows: int = 0) -> LmoeConfig:
     """C config from an lmoe_inputs.LayerConfig-like object."""
     return LmoeConfig(d_model=cfg.d_model, d_latent=cfg.d_latent, n_experts=cfg.n_experts, top_k=cfg.top_k,
                       d_expert_ff=cfg.d_expert_ff, d_shared_ff=cfg.d_shared_ff,
@@ -153,7 +158,8 @@ def make_config(cfg, max_tokens: int) -> LmoeConfig:
                       act=LMOE_ACT_SITU if cfg.act == "situ" else LMOE_ACT_SWIGLU,
                       expert_wfmt=LMOE_W_MXFP4 if cfg.expert_wfmt == "mxfp4" else LMOE_W_FP8_BLOCK128,
                       max_tokens=int(max_tokens), act_terms=int(getattr(cfg, "act_terms", 2)),
-                      act_format=1 if getattr(cfg, "act_format", "e4m3") == "e2m1" else 0)
+                      act_format=1 if getattr(cfg, "act_format", "e4m3") == "e2m1" else 0,
+                      ep_size=int(ep_size), ep_rank=int(ep_rank), max_recv_rows=int(max_recv_rows))
 
 
 class LatentMoE:
@@ -164,7 +170,8 @@ class LatentMoE:
     tensors are borrowed: this object keeps references so they outlive the
     handle."""
 
-    def __init__(self, cfg, weights: dict, max_tokens: int, stream=None):
+    def __init__(self, cfg, weights: dict, max_tokens: int, stream=None, ep_size: int = 1, ep_rank: int = 0,
+                 max_recv_rows: int = 0):
         lib = load_library()
         if not torch.cuda.is_available():
             raise RuntimeError("lmoe needs a CUDA GPU; no CPU implementation exists")
@@ -176,7 +183,8 @@ class LatentMoE:
                 raise ValueError(f"weight {k} must be a contiguous CUDA tensor")
         w = LmoeWeights(**{n: (self._weights[n].data_ptr() if n in self._weights else None)
                            for n in _WEIGHT_FIELDS})
-        c = make_config(cfg, max_tokens)
+        c = make_config(cfg, max_tokens, ep_size, ep_rank, max_recv_rows)
+        self.ep_size = max(1, int(ep_size))
         h = ctypes.c_void_p()
         _check("lmoe_create", lib.lmoe_create(ctypes.byref(c), ctypes.byref(w), _stream(stream), ctypes.byref(h)))
         self._h = h
@@ -260,6 +268,30 @@ class LatentMoE:
         _check("lmoe_qb_update_from_histogram", self._lib.lmoe_qb_update_from_histogram(
             self._h, _ptr(counts), counts.shape[1], _ptr(bias), _ptr(nb), _stream(stream)))
         return nb
+
+    # -- expert parallelism: the device phases between the caller's exchanges
+    def lmoe_ep_dispatch(self, x: torch.Tensor, stream=None):
+        """-> (send rows bf16 [T*k][dx] grouped by global expert, expert_counts int32 [E])."""
+        c = self.cfg
+        T = x.shape[0]
+        dx = c.d_latent or c.d_model
+        send = torch.empty(T * c.top_k, dx, dtype=torch.bfloat16, device=x.device)
+        counts = torch.empty(c.n_experts, dtype=torch.int32, device=x.device)
+        _check("lmoe_ep_dispatch", self._lib.lmoe_ep_dispatch(self._h, _ptr(x), T, _ptr(send), _ptr(counts), None,
+                                                              None, _stream(stream)))
+        return send, counts
+
+    def lmoe_ep_experts(self, recv: torch.Tensor, recv_counts: torch.Tensor, stream=None) -> torch.Tensor:
+        """Received rows bf16 [n][dx] and counts int32 [ep_size][E/ep_size] -> expert outputs bf16 [n][dx]."""
+        out = torch.empty_like(recv)
+        _check("lmoe_ep_experts", self._lib.lmoe_ep_experts(self._h, _ptr(recv), _ptr(recv_counts), recv.shape[0],
+                                                            _ptr(out), _stream(stream)))
+        return out
+
+    def lmoe_ep_combine(self, ret: torch.Tensor, T: int, stream=None) -> torch.Tensor:
+        out = torch.empty(T, self.cfg.d_model, dtype=torch.bfloat16, device=ret.device)
+        _check("lmoe_ep_combine", self._lib.lmoe_ep_combine(self._h, _ptr(ret), int(T), _ptr(out), _stream(stream)))
+        return out
 
     def lmoe_sync_status(self, stream=None):
         _check("lmoe_sync_status", self._lib.lmoe_sync_status(self._h, _stream(stream)))

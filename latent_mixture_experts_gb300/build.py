@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "liblmoe.so")
-SOURCES = ["dense_gemm.cu", "routing.cu", "moe_gemm.cu", "moe_fp8.cu", "moe_fp4.cu", "lmoe_api.cu", "dispatch_noalloc.cu", "selftest.cu", "tc_peak.cu", "quantile_balance.cu"]
+SOURCES = ["dense_gemm.cu", "routing.cu", "moe_gemm.cu", "moe_fp8.cu", "moe_fp4.cu", "lmoe_api.cu", "dispatch_noalloc.cu", "selftest.cu", "tc_peak.cu", "quantile_balance.cu", "expert_parallel.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]

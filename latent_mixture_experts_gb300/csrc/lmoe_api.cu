@@ -37,7 +37,14 @@ struct lmoe_ctx {
   int dx = 0;          // width the routed experts read and write: the latent, or d for non-latent layers
   bool fp8 = false;    // experts in FP8 E4M3 with 128 x 128 fp32 block scales
   int terms = 2;       // activation terms per routed-expert input (E4M3: 2 hi + lo, 1 MXFP8; E2M1: 1..4)
-  bool fp4 = false;    // packed E2M1 activations x MXFP4 weights (kind::mxf4nvf4); K padded to 256
+  bool fp4 = false;    // packed E2M1 activations x MXFP4 weights (kind::mxf4); K padded to 256
+  // expert parallelism: this handle holds experts [ep_rank * E_loc, (ep_rank + 1) * E_loc)
+  int ep = 1, ep_rank = 0, E_loc = 0;
+  int Pexp = 0;        // rows the expert GEMMs may see: T*k, or the rows received from all ranks
+  int32_t* ep_perm = nullptr;   // assignments grouped by global expert (the send order), kept for the combine
+  int32_t* idx_loc = nullptr;   // local expert of each received row
+  float* ones = nullptr;        // unit routing weights of the received rows
+  int ep_T = 0;                 // tokens of the last lmoe_ep_dispatch
   // FP8 layers run the shared expert on the FP8 expert GEMMs, as one expert
   // that every token uses (exact block-scaled weights): its tile list, identity
   // rows and unit weights, hi/lo activations and its fp32 output.
@@ -119,6 +126,12 @@ lmoe_status cuda_status(cudaError_t e) {
     if (e_ != cudaSuccess) return cuda_status(e_);       \
   } while (0)
 
+#define LMOE_TRY_STATUS(expr)                          \
+  do {                                                 \
+    const lmoe_status s_ = (expr);                     \
+    if (s_ != LMOE_OK) return s_;                      \
+  } while (0)
+
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -126,11 +139,12 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 constexpr int kRouterMaxSplits = 16;
 
 int dense_bn(int T) { return T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
-int moe_bn(int T, int k, int E) { return moe_tile_tokens(static_cast<long long>(T) * k, E); }
-// Token tile of the routed expert GEMMs of this handle's weight format.
-int expert_bn(const lmoe_ctx* h, int T) {
-  return h->fp8 ? fp8_tile_tokens(static_cast<long long>(T) * h->k, h->E) : moe_bn(T, h->k, h->E);
+// Token tile of the routed expert GEMMs of this handle's weight format for P
+// rows over its E_loc experts.
+int expert_bn_rows(const lmoe_ctx* h, long long P) {
+  return h->fp8 ? fp8_tile_tokens(P, h->E_loc) : moe_tile_tokens(P, h->E_loc);
 }
+int expert_bn(const lmoe_ctx* h, int T) { return expert_bn_rows(h, static_cast<long long>(T) * h->k); }
 
 // K splits of the routed MXFP4 expert GEMMs (1 = none) for a batch of P
 // assignments: when the weight-row items of a pass (an upper bound of its
@@ -140,12 +154,12 @@ int expert_bn(const lmoe_ctx* h, int T) {
 constexpr long long kKsplitMaxP = 1024;
 int expert_ksplit(const lmoe_ctx* h, long long P, bool gate_up) {
   if (h->fp8 || P > kKsplitMaxP) return 1;
-  const int BN = moe_tile_tokens(P, h->E);
+  const int BN = moe_tile_tokens(P, h->E_loc);
   if (BN != 16) return 1;   // the K-split form is built for the 16-assignment tile
   const int RB = moe_rows_per_item(BN);
   const long long MT = gate_up ? ceil_div(h->F, RB) : ceil_div(h->dx, 2 * RB);
   const int KG = (gate_up ? h->KG_gu : h->KG_dn) / (h->fp4 ? 2 : 1);   // K groups of the kernel that runs
-  const long long tiles = std::min<long long>(P, P / BN + std::min<long long>(h->E, P));
+  const long long tiles = std::min<long long>(P, P / BN + std::min<long long>(h->E_loc, P));
   const long long items = tiles * MT;
   if (items >= 2LL * h->num_sms) return 1;
   const long long want = 4LL * h->num_sms;
@@ -305,7 +319,9 @@ lmoe_status run_router(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& 
 }
 
 lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t* counts, int32_t* offsets,
-                         int32_t* perm, cudaStream_t st, int& launches) {
+                         int32_t* perm, cudaStream_t st, int& launches, int k = 0, int E = 0) {
+  k = k ? k : h->k;
+  E = E ? E : h->E;
   StageTimer tm(h, LMOE_STAGE_DISPATCH, st);
   DispatchBufs b;
   b.counts = counts;
@@ -317,8 +333,8 @@ lmoe_status run_dispatch(lmoe_ctx* h, const int32_t* idx, int T, int BN, int32_t
   b.tiles = h->tiles;
   b.ntiles = h->ntiles;
   b.err = h->err;
-  LMOE_TRY(launch_dispatch(idx, T, h->k, h->E, BN, b, st));
-  launches += dispatch_launches(T * h->k);
+  LMOE_TRY(launch_dispatch(idx, T, k, E, BN, b, st));
+  launches += dispatch_launches(T * k);
   tm.done();
   return LMOE_OK;
 }
@@ -343,6 +359,9 @@ lmoe_status validate_cfg(const lmoe_config* c) {
   if (c->act_terms < 0 || c->act_terms > (c->act_format == LMOE_ACT_FMT_E2M1 ? 4 : 2)) return LMOE_ERR_INVALID_ARG;
   if (c->act_terms == 1 && c->expert_wfmt != LMOE_W_MXFP4) return LMOE_ERR_UNSUPPORTED;
   if (c->act_format == LMOE_ACT_FMT_E2M1 && c->expert_wfmt != LMOE_W_MXFP4) return LMOE_ERR_UNSUPPORTED;
+  if (c->ep_size < 0 || c->ep_rank < 0 || c->max_recv_rows < 0) return LMOE_ERR_INVALID_ARG;
+  if (c->ep_size > 1 && (c->ep_rank >= c->ep_size || c->n_experts % c->ep_size)) return LMOE_ERR_INVALID_ARG;
+  if (c->ep_size > 1 && c->act_format == LMOE_ACT_FMT_E2M1) return LMOE_ERR_UNSUPPORTED;
   return LMOE_OK;
 }
 
@@ -431,10 +450,18 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   h->KG_dn = h->Fp / 128;
   h->Tm = cfg->max_tokens;
   h->Pm = h->Tm * h->k;
-  const int bn_max = expert_bn(h, h->Tm);
-  h->Ppad = h->Pm + h->E * (bn_max - 1);
-  h->max_tiles = h->Pm / 16 + h->E + 1;
-  h->nchunks_max = ceil_div(h->Pm, kDispatchChunk);
+  h->ep = cfg->ep_size > 1 ? cfg->ep_size : 1;
+  h->ep_rank = h->ep > 1 ? cfg->ep_rank : 0;
+  h->E_loc = h->E / h->ep;
+  // rows the expert GEMMs may see: the batch's own assignments, or under
+  // expert parallelism the rows received from every rank
+  h->Pexp = h->ep > 1 ? static_cast<int>(cfg->max_recv_rows ? cfg->max_recv_rows
+                                                            : std::min<long long>(1LL << 30, 1LL * h->ep * h->Pm))
+                      : h->Pm;
+  const int bn_max = expert_bn_rows(h, h->Pexp);
+  h->Ppad = h->Pexp + h->E_loc * (bn_max - 1);
+  h->max_tiles = std::max(h->Pexp / 16 + h->E_loc, h->Pm / 16 + h->E) + 1;
+  h->nchunks_max = ceil_div(std::max(h->Pm, h->Pexp), kDispatchChunk);
 
   // dense partial buffer: max over the four GEMMs of splits * T * ld
   long long part_elems = 0;
@@ -459,14 +486,14 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const size_t xsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_gu * atoms_per * 512;
   const size_t hsf_bytes = static_cast<size_t>(ceil_div(h->Ppad, 16)) * h->KG_dn * atoms_per * 512;
   const bool pad_gu = !h->fp8 && h->Kp != h->dx, pad_dn = !h->fp8 && h->Fp != h->F;
-  const size_t sfa_gu_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_gu * h->KG_gu * 512;
-  const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E) * h->MTa_dn * h->KG_dn * 512;
+  const size_t sfa_gu_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E_loc) * h->MTa_gu * h->KG_gu * 512;
+  const size_t sfa_dn_bytes = h->fp8 ? 0 : static_cast<size_t>(h->E_loc) * h->MTa_dn * h->KG_dn * 512;
   const bool sh8 = h->fp8 && h->Fs;   // shared expert on the FP8 expert GEMMs
   h->Tpad_sh = sh8 ? h->Tm + kFp8MaxTile : 0;
   // K-split scratch: partial gate/up sums, arrival counters (fewer than
   // 4 * SMs items when split), and room for the down pass's partial planes
-  long long gpart_elems = 0, y_rows = h->Pm;
-  for (long long P = 1; P <= std::min<long long>(h->Pm, kKsplitMaxP); ++P) {
+  long long gpart_elems = 0, y_rows = std::max(h->Pm, h->Pexp);
+  for (long long P = 1; P <= std::min<long long>(h->Pexp, kKsplitMaxP); ++P) {
     const int kg = expert_ksplit(h, P, true), kd = expert_ksplit(h, P, false);
     if (kg > 1) gpart_elems = std::max(gpart_elems, 2LL * kg * P * h->F);
     y_rows = std::max(y_rows, static_cast<long long>(kd) * P);
@@ -486,9 +513,14 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->counts = c.take<int32_t>(h->E, base);
     h->offsets = c.take<int32_t>(h->E + 1, base);
     h->tile_off = c.take<int32_t>(h->E + 1, base);
-    h->perm = c.take<int32_t>(h->Pm, base);
-    h->inv_pad = c.take<int32_t>(h->Pm, base);
+    h->perm = c.take<int32_t>(std::max(h->Pm, h->Pexp), base);
+    h->inv_pad = c.take<int32_t>(std::max(h->Pm, h->Pexp), base);
     h->blockcnt = c.take<int32_t>(static_cast<size_t>(h->nchunks_max) * h->E, base);
+    if (h->ep > 1) {
+      h->ep_perm = c.take<int32_t>(h->Pm, base);
+      h->idx_loc = c.take<int32_t>(h->Pexp, base);
+      h->ones = c.take<float>(h->Pexp, base);
+    }
     h->ntiles = c.take<int32_t>(1, base);
     h->tiles = c.take<int4>(h->max_tiles, base);
     h->xq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Kp, base);
@@ -520,10 +552,10 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
       h->y_sh = c.take<float>(static_cast<size_t>(h->Tm) * h->d, base);
     }
     if (pad_gu) {
-      h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
-      h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E) * h->F * (h->Kp / 2), base);
+      h->pad_gate = c.take<uint8_t>(static_cast<size_t>(h->E_loc) * h->F * (h->Kp / 2), base);
+      h->pad_up = c.take<uint8_t>(static_cast<size_t>(h->E_loc) * h->F * (h->Kp / 2), base);
     }
-    if (pad_dn) h->pad_down = c.take<uint8_t>(static_cast<size_t>(h->E) * h->din * (h->Fp / 2), base);
+    if (pad_dn) h->pad_down = c.take<uint8_t>(static_cast<size_t>(h->E_loc) * h->din * (h->Fp / 2), base);
     h->qb_alpha = c.take<float>(h->Tm, base);
     h->qb_raw = c.take<float>(h->E, base);
     h->qb_range = c.take<float>(2, base);
@@ -562,25 +594,26 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   const uint8_t* su = static_cast<const uint8_t*>(w->ex_up_s);
   const uint8_t* sd = static_cast<const uint8_t*>(w->ex_down_s);
   if (!h->fp8 &&
-      (launch_relayout_sfa(sg, h->E, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
-       launch_relayout_sfa(su, h->E, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
-       launch_relayout_sfa(sd, h->E, h->dx, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess))
+      (launch_relayout_sfa(sg, h->E_loc, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_gate, stream) != cudaSuccess ||
+       launch_relayout_sfa(su, h->E_loc, h->F, h->dx / 32, h->MTa_gu, h->KG_gu, h->sfa_up, stream) != cudaSuccess ||
+       launch_relayout_sfa(sd, h->E_loc, h->dx, h->F / 32, h->MTa_dn, h->KG_dn, h->sfa_down, stream) != cudaSuccess))
     return fail(LMOE_ERR_CUDA);
   if (sh8 && launch_iota_ones(h->sh_iota, h->sh_ones, h->Tm, stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
+  if (h->ones && launch_iota_ones(h->idx_loc, h->ones, h->Pexp, stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
   if (h->sh_gu_il && launch_interleave_gate_up(w->sh_gate, w->sh_up, h->Fs, h->d, h->sh_gu_il, stream) != cudaSuccess)
     return fail(LMOE_ERR_CUDA);
   h->codes_gate = w->ex_gate_q;
   h->codes_up = w->ex_up_q;
   h->codes_down = w->ex_down_q;
   if (pad_gu) {
-    if (launch_pad_codes(w->ex_gate_q, h->E, h->F, h->din, h->Kp, h->pad_gate, stream) != cudaSuccess ||
-        launch_pad_codes(w->ex_up_q, h->E, h->F, h->din, h->Kp, h->pad_up, stream) != cudaSuccess)
+    if (launch_pad_codes(w->ex_gate_q, h->E_loc, h->F, h->din, h->Kp, h->pad_gate, stream) != cudaSuccess ||
+        launch_pad_codes(w->ex_up_q, h->E_loc, h->F, h->din, h->Kp, h->pad_up, stream) != cudaSuccess)
       return fail(LMOE_ERR_CUDA);
     h->codes_gate = h->pad_gate;
     h->codes_up = h->pad_up;
   }
   if (pad_dn) {
-    if (launch_pad_codes(w->ex_down_q, h->E, h->din, h->F, h->Fp, h->pad_down, stream) != cudaSuccess)
+    if (launch_pad_codes(w->ex_down_q, h->E_loc, h->din, h->F, h->Fp, h->pad_down, stream) != cudaSuccess)
       return fail(LMOE_ERR_CUDA);
     h->codes_down = h->pad_down;
   }
@@ -612,17 +645,17 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
   for (int i = 0; i < 2; ++i) {
     const int rows = 128 << i;
     if (h->fp8) {
-      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->dx, rows);
+      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E_loc) * h->dx, rows);
     } else if (h->fp4) {   // packed codes as bytes: a 128-byte box row is 256 K values
-      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp / 2, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp / 2, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp / 2, static_cast<long long>(h->E) * h->dx, rows);
+      ok &= map_u8(&h->m_exg[i], h->codes_gate, h->Kp / 2, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_u8(&h->m_exu[i], h->codes_up, h->Kp / 2, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_u8(&h->m_exd[i], h->codes_down, h->Fp / 2, static_cast<long long>(h->E_loc) * h->dx, rows);
     } else {
-      ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E) * h->F, rows);
-      ok &= map_fp4(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E) * h->dx, rows);
+      ok &= map_fp4(&h->m_exg[i], h->codes_gate, h->Kp, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_fp4(&h->m_exu[i], h->codes_up, h->Kp, static_cast<long long>(h->E_loc) * h->F, rows);
+      ok &= map_fp4(&h->m_exd[i], h->codes_down, h->Fp, static_cast<long long>(h->E_loc) * h->dx, rows);
     }
   }
   if (!ok) return fail(LMOE_ERR_CUDA);
@@ -729,20 +762,14 @@ lmoe_status lmoe_dispatch(lmoe_handle h, const int32_t* topk_idx, int T, int32_t
   return run_dispatch(h, topk_idx, T, expert_bn(h, T), counts, offsets, perm, st, launches);
 }
 
-lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t* topk_idx_opt, float* topk_w_opt,
-                         cudaStream_t st) {
-  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
-  if (T == 0) return LMOE_OK;
-  if (!x || !out || !aligned(x, 16) || !aligned(out, 16) || x == out) return LMOE_ERR_INVALID_ARG;
-  int launches = 0;
-  const int d = h->d, din = h->din, dx = h->dx, Fs = h->Fs;
+// Steps 4 and 9 on the handle's side stream, forked from `st`: the latent
+// down-projection (ev_latent) and the shared expert (ev_join), which need
+// only x and overlap the router, dispatch and routed experts.
+static lmoe_status run_side(lmoe_ctx* h, const void* x, int T, cudaStream_t st, int& launches) {
+  const int d = h->d, din = h->din, Fs = h->Fs;
   const int BN = dense_bn(T);
   const int nt = ceil_div(T, BN);
   const int nkb_d = ceil_div(d, 64);
-  begin_call(h);
-
-  // Side stream: the steps that need only x overlap the router, dispatch and
-  // routed experts of the caller's stream.
   cudaStream_t ss = h->side;
   if (ss) {
     LMOE_TRY(cudaEventRecord(h->ev_fork, st));
@@ -874,35 +901,16 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     tm.done();
     LMOE_TRY(cudaEventRecord(h->ev_join, ss));
   }
-  // 1-2 router
-  lmoe_status s = run_router(h, x, T, st, launches);
-  if (s != LMOE_OK) return s;
-  // 3 dispatch
-  const int BNm = expert_bn(h, T);
-  const int split = h->fp8 || moe_split(BNm);   // activation layout the expert GEMMs read
-  s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
-  if (s != LMOE_OK) return s;
+  return LMOE_OK;
+}
 
-  const int KSg = expert_ksplit(h, static_cast<long long>(T) * h->k, true);
-  if (din) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_latent, 0));   // x^c from the side stream
-  // 5 activations -> hi/lo E4M3 in expert-tile order
-  {
-    StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
-    if (h->fp4)
-      LMOE_TRY(launch_quant_gather_fp4(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->terms, h->xq, h->xsf, h->sched,
-                                       h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
-    else if (din)
-      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
-                                   h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
-    else
-      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
-                                        h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
-    ++launches;
-    tm.done();
-  }
-  // 6-7 routed experts (small batches K split)
-  const long long P = static_cast<long long>(T) * h->k;
-  const int KSd = expert_ksplit(h, P, false);
+// Steps 6-7: the grouped gate/up and down GEMMs over the tiles of the last
+// dispatch (P rows, routing weights G per row); the K splits of the down pass
+// (planes of P x dx in y) are returned in KSd.
+static lmoe_status run_experts(lmoe_ctx* h, long long P, int BNm, int split, const float* G, cudaStream_t st, int& launches,
+                        int& KSd) {
+  const int dx = h->dx;
+  KSd = expert_ksplit(h, P, false);
   {
     MoeGemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -926,7 +934,7 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     p.tile_off = h->tile_off;
     p.ntiles = h->ntiles;
     p.perm = h->perm;
-    p.G = h->G;
+    p.G = G;
     p.err = h->err;
     p.sched = h->sched;
     p.KS = expert_ksplit(h, P, true);
@@ -982,6 +990,16 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     ++launches;
     tdn.done();
   }
+  return LMOE_OK;
+}
+
+// Steps 8 and 10: the slot-ordered sum of y (KSd planes) with the latent
+// RMSNorm, then Delta = u_hat W_up^T + h_shared W_shared_down^T (latent
+// layers) or the routed sum plus the shared expert (non-latent layers).
+static lmoe_status run_combine_output(lmoe_ctx* h, int T, long long P, int KSd, void* out, cudaStream_t st, int& launches) {
+  const int d = h->d, din = h->din, dx = h->dx, Fs = h->Fs;
+  const int BN = dense_bn(T);
+  const int nt = ceil_div(T, BN);
   // 8 expert sum in slot order + latent RMSNorm
   {
     StageTimer tm(h, LMOE_STAGE_COMBINE, st);
@@ -1046,6 +1064,50 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
     }
     tm.done();
   }
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t* topk_idx_opt, float* topk_w_opt,
+                         cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !out || !aligned(x, 16) || !aligned(out, 16) || x == out) return LMOE_ERR_INVALID_ARG;
+  if (h->ep > 1) return LMOE_ERR_UNSUPPORTED;   // expert-parallel handles run the lmoe_ep_* phases
+  int launches = 0;
+  const int d = h->d, din = h->din;
+  begin_call(h);
+
+  LMOE_TRY_STATUS(run_side(h, x, T, st, launches));
+  // 1-2 router
+  lmoe_status s = run_router(h, x, T, st, launches);
+  if (s != LMOE_OK) return s;
+  // 3 dispatch
+  const int BNm = expert_bn(h, T);
+  const int split = h->fp8 || moe_split(BNm);   // activation layout the expert GEMMs read
+  s = run_dispatch(h, h->idx, T, BNm, h->counts, h->offsets, h->perm, st, launches);
+  if (s != LMOE_OK) return s;
+
+  const int KSg = expert_ksplit(h, static_cast<long long>(T) * h->k, true);
+  if (din) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_latent, 0));   // x^c from the side stream
+  // 5 activations -> hi/lo E4M3 in expert-tile order
+  {
+    StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
+    if (h->fp4)
+      LMOE_TRY(launch_quant_gather_fp4(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, h->terms, h->xq, h->xsf, h->sched,
+                                       h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+    else if (din)
+      LMOE_TRY(launch_quant_gather(h->xc, T, h->k, din, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
+                                   h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+    else
+      LMOE_TRY(launch_quant_gather_bf16(x, T, h->k, d, h->Kp, h->inv_pad, BNm, split, h->terms, h->xq, h->xsf,
+                                        h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+    ++launches;
+    tm.done();
+  }
+  const long long P = static_cast<long long>(T) * h->k;
+  int KSd = 1;
+  LMOE_TRY_STATUS(run_experts(h, P, BNm, split, h->G, st, launches, KSd));
+  LMOE_TRY_STATUS(run_combine_output(h, T, P, KSd, out, st, launches));
   const size_t n = static_cast<size_t>(T) * h->k;
   if (topk_idx_opt) LMOE_TRY(cudaMemcpyAsync(topk_idx_opt, h->idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
   if (topk_w_opt) LMOE_TRY(cudaMemcpyAsync(topk_w_opt, h->G, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
@@ -1053,6 +1115,75 @@ lmoe_status lmoe_forward(lmoe_handle h, const void* x, int T, void* out, int32_t
   h->last_launches = launches;
   h->last_BN = BNm;
   h->last_split = split;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_ep_dispatch(lmoe_handle h, const void* x, int T, void* send_bf16, int32_t* expert_counts,
+                             int32_t* topk_idx_opt, float* topk_w_opt, cudaStream_t st) {
+  if (!h || T < 0 || T > h->Tm) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !aligned(x, 16) || !send_bf16 || !aligned(send_bf16, 16) || !expert_counts || !h->ep_perm)
+    return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  begin_call(h);
+  LMOE_TRY_STATUS(run_side(h, x, T, st, launches));
+  LMOE_TRY_STATUS(run_router(h, x, T, st, launches));
+  // group the assignments by global expert: the rows for each rank become contiguous
+  LMOE_TRY_STATUS(run_dispatch(h, h->idx, T, 16, expert_counts, h->offsets, h->ep_perm, st, launches));
+  if (h->din) LMOE_TRY(cudaStreamWaitEvent(st, h->ev_latent, 0));
+  LMOE_TRY(launch_ep_pack(h->din ? h->xc : nullptr, h->din ? nullptr : x, h->dx, h->k, h->ep_perm, T * h->k,
+                          send_bf16, st));
+  ++launches;
+  const size_t n = static_cast<size_t>(T) * h->k;
+  if (topk_idx_opt) LMOE_TRY(cudaMemcpyAsync(topk_idx_opt, h->idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+  if (topk_w_opt) LMOE_TRY(cudaMemcpyAsync(topk_w_opt, h->G, n * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  h->ep_T = T;
+  h->last_launches = launches;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_ep_experts(lmoe_handle h, const void* recv_bf16, const int32_t* recv_counts, int n, void* out_bf16,
+                            cudaStream_t st) {
+  if (!h || !h->idx_loc || n < 0 || n > h->Pexp) return LMOE_ERR_INVALID_ARG;
+  if (!recv_counts) return LMOE_ERR_INVALID_ARG;
+  if (n == 0) return LMOE_OK;
+  if (!recv_bf16 || !aligned(recv_bf16, 16) || !out_bf16 || !aligned(out_bf16, 16)) return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  begin_call(h);
+  // the local expert of each received row, then the same grouping and tiles as a local batch of n rows, k = 1
+  LMOE_TRY(launch_ep_expand(recv_counts, h->ep * h->E_loc, h->E_loc, n, h->idx_loc, h->err, st));
+  const int BN = expert_bn_rows(h, n);
+  const int split = h->fp8 || moe_split(BN);
+  LMOE_TRY_STATUS(run_dispatch(h, h->idx_loc, n, BN, h->counts, h->offsets, h->perm, st, launches, 1, h->E_loc));
+  const int KSg = expert_ksplit(h, n, true);
+  {
+    StageTimer tm(h, LMOE_STAGE_ACT_QUANT, st);
+    LMOE_TRY(launch_quant_gather_bf16(recv_bf16, n, 1, h->dx, h->Kp, h->inv_pad, BN, split, h->terms, h->xq, h->xsf,
+                                      h->sched, h->gcnt, KSg > 1 ? h->n_gcnt : 0, st));
+    ++launches;
+    tm.done();
+  }
+  int KSd = 1;
+  LMOE_TRY_STATUS(run_experts(h, n, BN, split, h->ones, st, launches, KSd));
+  LMOE_TRY(launch_ep_cast(h->y, n, h->dx, KSd, static_cast<size_t>(n) * h->dx, out_bf16, st));
+  launches += 2;
+  h->last_launches = launches + 1;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_ep_combine(lmoe_handle h, const void* ret_bf16, int T, void* out_bf16, cudaStream_t st) {
+  if (!h || !h->ep_perm || T < 0 || T != h->ep_T) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!ret_bf16 || !aligned(ret_bf16, 16) || !out_bf16 || !aligned(out_bf16, 16)) return LMOE_ERR_INVALID_ARG;
+  int launches = 0;
+  begin_call(h);
+  const long long P = static_cast<long long>(T) * h->k;
+  // returned expert outputs back in assignment order, weighted by G, for the slot-ordered sum
+  LMOE_TRY(launch_ep_unpack(ret_bf16, static_cast<int>(P), h->dx, h->ep_perm, h->G, h->y, st));
+  ++launches;
+  LMOE_TRY_STATUS(run_combine_output(h, T, P, 1, out_bf16, st, launches));
+  h->last_T = T;
+  h->last_launches = launches;
   return LMOE_OK;
 }
 

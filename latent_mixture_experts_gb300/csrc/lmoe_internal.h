@@ -248,6 +248,21 @@ cudaError_t launch_qb_histogram(const float* z, int T, int E, int k, const float
 cudaError_t launch_qb_from_histogram(const int32_t* counts, int E, int bins, int k, const float* bias, float* range,
                                      float* raw, float* new_bias, cudaStream_t s);
 
+// ------------------------------------------------------ expert parallelism
+// send[pos] = bf16 row of the token of assignment perm[pos]: from x^c (fp32,
+// latent layers) or from x (bf16 xb, non-latent layers), P rows of dx.
+cudaError_t launch_ep_pack(const float* xc, const void* xb, int dx, int k, const int32_t* perm, int P, void* send,
+                           cudaStream_t s);
+// idx_loc[row] = local expert of received row `row` (< n), from counts [nseg]
+// (source rank major, E_loc experts each); err[1] = 1 when they do not sum to n.
+cudaError_t launch_ep_expand(const int32_t* counts, int nseg, int E_loc, int n, int32_t* idx_loc, int* err,
+                             cudaStream_t s);
+// out[row] = bf16(sum over ks planes of y[row]) for n rows of dx.
+cudaError_t launch_ep_cast(const float* y, int n, int dx, int ks, size_t plane, void* out, cudaStream_t s);
+// y[perm[pos]] = G[perm[pos]] * ret[pos] (bf16 rows) for P rows of dx.
+cudaError_t launch_ep_unpack(const void* ret, int P, int dx, const int32_t* perm, const float* G, float* y,
+                             cudaStream_t s);
+
 // One warp waits on an mbarrier nothing arrives at, with the given limit;
 // the bounded wait then records kErrTimeout in err[0].
 cudaError_t launch_wait_timeout_probe(int* err, unsigned long long limit_ns, cudaStream_t s);

@@ -90,6 +90,10 @@ def test_create_rejects_bad_arguments(lib):
     assert _create(lib, _cfg(), _weights(skip=("ex_up_q",)))[0] == b.LMOE_ERR_INVALID_ARG
     assert _create(lib, _cfg(), _weights(skip=("norm_w",)))[0] == b.LMOE_ERR_INVALID_ARG
     assert _create(lib, _cfg(act_terms=3), _weights())[0] == b.LMOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(act_format=1, act_terms=5), _weights())[0] == b.LMOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(ep_size=3), _weights())[0] == b.LMOE_ERR_INVALID_ARG      # 64 experts over 3 ranks
+    assert _create(lib, _cfg(ep_size=2, ep_rank=2), _weights())[0] == b.LMOE_ERR_INVALID_ARG
+    assert _create(lib, _cfg(ep_size=2, act_format=1), _weights())[0] == b.LMOE_ERR_UNSUPPORTED
     assert _create(lib, _cfg(act_terms=1, expert_wfmt=1, d_latent=0, use_latent_norm=0),
                    _weights())[0] == b.LMOE_ERR_UNSUPPORTED     # one-term activations: MXFP4 experts only
     w = _weights()
@@ -116,6 +120,10 @@ def test_null_handle_calls(lib):
     assert lib.lmoe_last_launch_count(None) == 0
     assert lib.lmoe_keep_f32_output(None, 1) == b.LMOE_ERR_INVALID_ARG
     assert lib.lmoe_selftest_timeout(None, 5000, None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_ep_dispatch(None, None, 1, None, None, None, None, None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_ep_experts(None, None, None, 1, None, None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_ep_combine(None, None, 1, None, None) == b.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_qb_update(None, None, 1, None, None, None) == b.LMOE_ERR_INVALID_ARG
 
 
 def test_tc_peak_rejects_bad_arguments(lib):
