@@ -516,11 +516,10 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, cudaStrea
     h->perm = c.take<int32_t>(std::max(h->Pm, h->Pexp), base);
     h->inv_pad = c.take<int32_t>(std::max(h->Pm, h->Pexp), base);
     h->blockcnt = c.take<int32_t>(static_cast<size_t>(h->nchunks_max) * h->E, base);
-    if (h->ep > 1) {
-      h->ep_perm = c.take<int32_t>(h->Pm, base);
-      h->idx_loc = c.take<int32_t>(h->Pexp, base);
-      h->ones = c.take<float>(h->Pexp, base);
-    }
+    // expert-parallel phases (also on a single rank, where they run every expert locally)
+    h->ep_perm = c.take<int32_t>(h->Pm, base);
+    h->idx_loc = c.take<int32_t>(h->Pexp, base);
+    h->ones = c.take<float>(h->Pexp, base);
     h->ntiles = c.take<int32_t>(1, base);
     h->tiles = c.take<int4>(h->max_tiles, base);
     h->xq = c.take<uint8_t>(2 * static_cast<size_t>(h->Ppad) * h->Kp, base);
