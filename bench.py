@@ -440,7 +440,10 @@ def run_per_config(args, pk, tc, budget_s: float = 240.0) -> list:
 
 
 def with_activation_format(wl, args):
-    """The workload with the command line's activation format / terms, if given."""
+    """The workload with the command line's activation format / terms / token
+    count, if given."""
+    if getattr(args, "T", None):
+        wl = replace(wl, T=args.T, name=f"{wl.name}_T{args.T}")
     over = {}
     if getattr(args, "act_format", None):
         over["act_format"] = args.act_format
@@ -694,6 +697,7 @@ def main():
     ap.add_argument("--act-format", choices=["e4m3", "e2m1"], default=None,
                     help="routed-expert activation format (default: the workload's)")
     ap.add_argument("--act-terms", type=int, default=None, help="activation terms (default: the workload's)")
+    ap.add_argument("--T", type=int, default=None, help="token count (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
