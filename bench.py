@@ -411,6 +411,15 @@ PER_CONFIG = (("k3_sweep", (1, 8, 32, 128, 512, 2048)), ("k3_prefill_t8192", Non
               ("k3_prefill_t8192_mxfp8", None), ("k2_t4096", None))
 
 
+def expert_dtype(cfg) -> str:
+    """The operand types of the routed-expert MMAs."""
+    if cfg.expert_wfmt != "mxfp4":
+        return "e4m3 x e4m3(hi+lo), fp32 block-128 scales" if cfg.act_terms == 2 else "e4m3 x e4m3, fp32 block-128 scales"
+    if getattr(cfg, "act_format", "e4m3") == "e2m1":
+        return f"e2m1 x e2m1 ({cfg.act_terms} mxfp4 terms) block-scaled"
+    return "e2m1 x e4m3(hi+lo) block-scaled" if cfg.act_terms == 2 else "e2m1 x e4m3 (mxfp8) block-scaled"
+
+
 def run_per_config(args, pk, tc, budget_s: float = 240.0) -> list:
     import torch
     from lmoe_inputs import configs as C
@@ -544,9 +553,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": (("e2m1 x e4m3(hi+lo) block-scaled" if cfg.act_terms == 2 else "e2m1 x e4m3 (mxfp8) block-scaled")
-                  + "; bf16 dense; fp32 accumulate" if fp4 else
-                  "e4m3 x e4m3(hi+lo), fp32 block-128 scales; bf16 dense; fp32 accumulate"),
+        "dtype": expert_dtype(cfg) + "; bf16 dense; fp32 accumulate",
         "data": "synthetic (seeded, N(0,1/fan_in) weights quantised to "
                 + ("MXFP4" if fp4 else "FP8 E4M3 block-128") + "; x ~ N(0,1) bf16)",
         "config": {"workload": wl.name, "T": T, "d_model": cfg.d_model, "d_latent": cfg.d_latent, "n_experts": cfg.n_experts,
