@@ -71,6 +71,12 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
+// Largest of 32 non-negative values (one per lane), all lanes: the bit
+// patterns of non-negative floats order as unsigned integers, so one
+// warp-wide integer max reduction gives the float maximum exactly.
+__device__ __forceinline__ float warp_amax(float nonneg) {
+  return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(nonneg)));
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -87,11 +93,11 @@ struct HiLo {
 };
 __device__ __forceinline__ HiLo quant_hilo_warp(float a) {
   HiLo r;
-  const float amax = warp_max(fabsf(a));
+  const float amax = warp_amax(fabsf(a));
   r.s_hi = e4m3_block_scale(amax);
   r.q_hi = f32_to_e4m3(a * e8m0_to_f32(254u - r.s_hi));
   const float res = a - e4m3_to_f32(r.q_hi) * e8m0_to_f32(r.s_hi);
-  const float rmax = warp_max(fabsf(res));
+  const float rmax = warp_amax(fabsf(res));
   r.s_lo = e4m3_block_scale(rmax);
   r.q_lo = f32_to_e4m3(res * e8m0_to_f32(254u - r.s_lo));
   return r;
@@ -106,9 +112,7 @@ __device__ __forceinline__ void quant_hilo_warp_n(const float (&a)[N], HiLo (&r)
 #pragma unroll
   for (int u = 0; u < N; ++u) m[u] = fabsf(a[u]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+  for (int u = 0; u < N; ++u) m[u] = warp_amax(m[u]);
 #pragma unroll
   for (int u = 0; u < N; ++u) {
     r[u].s_hi = e4m3_block_scale(m[u]);
@@ -117,9 +121,7 @@ __device__ __forceinline__ void quant_hilo_warp_n(const float (&a)[N], HiLo (&r)
     m[u] = fabsf(res[u]);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+  for (int u = 0; u < N; ++u) m[u] = warp_amax(m[u]);
 #pragma unroll
   for (int u = 0; u < N; ++u) {
     r[u].s_lo = e4m3_block_scale(m[u]);
@@ -136,9 +138,7 @@ __device__ __forceinline__ void quant_hi_warp_n(const float (&a)[N], HiLo (&r)[N
 #pragma unroll
   for (int u = 0; u < N; ++u) m[u] = fabsf(a[u]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], off));
+  for (int u = 0; u < N; ++u) m[u] = warp_amax(m[u]);
 #pragma unroll
   for (int u = 0; u < N; ++u) {
     r[u].s_hi = e4m3_block_scale(m[u]);

@@ -122,9 +122,7 @@ __device__ __forceinline__ void encode_h_fp4(float (&h)[N], const int (&rr)[N], 
 #pragma unroll
     for (int u = 0; u < N; ++u) m[u] = fabsf(h[u]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int u = 0; u < N; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], o));
+    for (int u = 0; u < N; ++u) m[u] = warp_amax(m[u]);
 #pragma unroll
     for (int u = 0; u < N; ++u) {
       const uint32_t s = e2m1_block_scale(m[u]);
