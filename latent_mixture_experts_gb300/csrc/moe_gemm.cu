@@ -56,6 +56,8 @@ struct MoeCfg {
   static constexpr int kTmemUsed = kAccBufs * kAcc + kStages * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr int kAtoms = kNAcc + NA;           // scale atoms of a stage, in TMEM column order
+  static_assert(kSf == kAtoms * 512 && (kAtoms == 4 || kAtoms == 5), "one stage's atoms: 4 TMEM columns each");
   static_assert(kTile % 1024 == 0, "tiles keep 1024-byte alignment");
   static_assert(kTmemUsed <= 512, "tensor memory budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -164,15 +166,24 @@ __device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t 
   }
 }
 
+// Scale warps: one per TMEM lane quarter.  Each stage's E8M0 scale atoms go
+// from shared memory to the stage's tensor-memory columns by these warps'
+// tcgen05.st (every quarter holds the same 32 rows of an atom, as the MMA
+// reads them), so the MMA thread's tensor pipe runs MMAs only; a per-stage
+// tcgen05.cp ahead of the MMAs held the pipe ~25 ns per atom.
+constexpr int kScaleWarps = 4;
+constexpr int kMoeThreads = 64 + 32 * (kEpiWarps + kScaleWarps);   // TMA, MMA, epilogue x4, scales x4
+
 // KSP: the K-split form for small batches (p.KS splits per item); without it
 // p.KS is taken as 1.
 template <int BN, bool GU, bool KSP>
-__global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
+__global__ void __launch_bounds__(kMoeThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeGemmParams p) {
   using C = MoeCfg<BN, GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* sf_region = sm + C::kStages * C::kTile;
   __shared__ uint64_t full[C::kStages], empty[C::kStages], acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
+  __shared__ uint64_t sf_ready[C::kStages];   // the stage's scales are in tensor memory
   __shared__ uint32_t tmem_base;
   __shared__ ItemRing ring;
 
@@ -181,12 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&sf_ready[i], kScaleWarps * 32);
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiWarps * 32);
     }
-    ring_init(ring, kEpiWarps);
+    ring_init(ring, kEpiWarps + kScaleWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -281,20 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const uint32_t d0 = tbase + b * C::kAcc;
         for (int g = g0; g < g1; ++g, ++it) {
           const int s = it % C::kStages;
-          if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
+          // the stage's operands have landed and the scale warps have put its scales in tensor memory
+          if (!mbar_wait(&sf_ready[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          // accumulator i = box j, tile t reads scale columns sf + 4i; the activation atoms follow
           const uint32_t sf = tbase + C::kAccBufs * C::kAcc + s * C::kSfCols;
           const uint32_t sfb = sf + 4 * C::kNAcc;
-          // scale atoms -> TMEM: accumulator i = box j, tile t reads columns sf + 4i
-#pragma unroll
-          for (int i = 0; i < C::kNAcc; ++i)
-            tmem_cp_32x128b_x4(sf + 4 * i, sdesc_noswz(smem_u32(st_sfa(s, i / C::kTiles)) + 512 * (i % C::kTiles), 16, 128));
-#pragma unroll
-          for (int a = 0; a < C::NA; ++a)
-            if (a == 0 || !one) tmem_cp_32x128b_x4(sfb + 4 * a, sdesc_noswz(smem_u32(st_sfb(s)) + 512 * a, 16, 128));
           const uint32_t bb = smem_u32(st_b(s));
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
@@ -313,6 +320,45 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           mma_commit(&empty[s]);
         }
         mma_commit(&acc_full[b]);
+      }
+    }
+  } else if (warp >= 2 + kEpiWarps) {
+    // Scale warps: lane r of the warp on quarter q writes row r of each of the
+    // stage's atoms (16 bytes: the four k-block scales of four row groups) to
+    // the four columns of that atom, in the quarter's 32 lanes.
+    const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + C::kAccBufs * C::kAcc;
+    uint32_t it = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int w = ring_take_warp(ring, n, p.err);
+      if (w < 0) break;
+      int g0, g1;
+      krange(w, g0, g1);
+      for (int g = g0; g < g1; ++g, ++it) {
+        const int s = it % C::kStages;
+        if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err, kErrTimeout)) {
+          ok = false;
+          break;
+        }
+        const uint4* at = reinterpret_cast<const uint4*>(sf_region + s * C::kSf) + lane;
+        uint32_t r[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = at[32 * k];
+          r[4 * k] = v.x;
+          r[4 * k + 1] = v.y;
+          r[4 * k + 2] = v.z;
+          r[4 * k + 3] = v.w;
+        }
+        const uint32_t dst = col0 + s * C::kSfCols;
+        tmem_st16(dst, r);
+        if constexpr (C::kAtoms == 5) {
+          const uint4 v = at[32 * 4];
+          tmem_st4(dst + 16, v.x, v.y, v.z, v.w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sf_ready[s]);
       }
     }
   } else {
@@ -485,7 +531,7 @@ cudaError_t launch_moe_k(const MoeGemmParams& p, int grid, cudaStream_t s) {
                                        C::kSmem);
   if (e != cudaSuccess) return e;
   {
-    const cudaError_t e_ = launch_pdl(moe_gemm_kernel<BN, GU, KSP>, grid, kThreads, C::kSmem, s, p);
+    const cudaError_t e_ = launch_pdl(moe_gemm_kernel<BN, GU, KSP>, grid, kMoeThreads, C::kSmem, s, p);
     if (e_ != cudaSuccess) return e_;
   }
   return cudaGetLastError();
