@@ -51,11 +51,11 @@ UNIT = "tokens/s"
 # DRAM bytes (read + write) per algorithmic byte of the gate/up expert
 # kernel of each weight format, from one ncu capture of the kernel as it
 # stands on a small case of the same instantiation (K3 shapes with 64
-# experts at T = 8: 702.4 MB for 645.2 MB; at T = 1024, the prefill tile:
-# 996.7 MB for 974 MB; K2 shapes with 32 experts at T = 384: 1046.8 MB for
+# experts at T = 8: 702.2 MB for 645.2 MB; at T = 1024, the prefill tile:
+# 997.0 MB for 974 MB; K2 shapes with 32 experts at T = 384: 1033.2 MB for
 # 998.1 MB), keyed by (weight format, token tile).  An entry is removed when
 # its kernel changes until it is captured again.
-GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.089, ("mxfp4", 96): 1.023, ("fp8_block128", 96): 1.049}
+GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.088, ("mxfp4", 96): 1.024, ("fp8_block128", 96): 1.035}
 
 
 def expert_tile(cfg, T: int) -> int:
