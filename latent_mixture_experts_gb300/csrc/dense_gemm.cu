@@ -69,17 +69,18 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   griddep_launch();
-  griddep_wait();
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) griddep_wait();   // the producer waits after requesting its first weight tiles
   const uint32_t tacc = tmem_base;
 
-  if (warp == 0 && lane == 0) {
-    // TMA producer
+  if (producer) {
+    // TMA producer.  The weights are never written by an earlier kernel, so
+    // the first stages' weight tiles are requested before waiting for the
+    // preceding kernel; its tokens (the B tiles) only after.
     const CUtensorMap* am = MT == 2 ? (seg ? &p.a1w : &p.a0w) : (seg ? &p.a1 : &p.a0);
     tma_prefetch_desc(am);
     tma_prefetch_desc(&p.b0);
-    for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-      const int s = i % C::kStages;
-      if (i >= C::kStages && !mbar_wait(&empty[s], ((i / C::kStages) - 1) & 1, p.err, kErrTimeout)) break;
+    auto load = [&](int kb, int s, bool a_part) {
       const CUtensorMap* A = am;
       const CUtensorMap* B = &p.b0;
       int kc = kb * 64;
@@ -89,13 +90,27 @@ __global__ void __launch_bounds__(128, 1) dense_gemm_kernel(const __grid_constan
         kc = (kb - p.nkb0) * 64;
       }
       uint8_t* st = sm + s * C::kStage;
-      mbar_arrive_expect_tx(&full[s], C::kStage);
-      if (pair) {   // gate rows then up rows of features m0.. (one 256-row box of the interleaved copy)
+      if (!a_part) {
+        tma_load_2d(st + C::kA, B, &full[s], kc, n0);
+      } else if (pair) {   // gate rows then up rows of features m0.. (one 256-row box of the interleaved copy)
         tma_load_2d(st, &p.a0w, &full[s], kc, 2 * m0);
       } else {
         tma_load_2d(st, A, &full[s], kc, m0);
       }
-      tma_load_2d(st + C::kA, B, &full[s], kc, n0);
+    };
+    const int npre = kb1 - kb0 < C::kStages ? kb1 - kb0 : C::kStages;
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(&full[i], C::kStage);
+      load(kb0 + i, i, true);
+    }
+    griddep_wait();
+    for (int i = 0; i < npre; ++i) load(kb0 + i, i, false);
+    for (int kb = kb0 + npre, i = npre; kb < kb1; ++kb, ++i) {
+      const int s = i % C::kStages;
+      if (i >= C::kStages && !mbar_wait(&empty[s], ((i / C::kStages) - 1) & 1, p.err, kErrTimeout)) break;
+      mbar_arrive_expect_tx(&full[s], C::kStage);
+      load(kb, s, true);
+      load(kb, s, false);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer

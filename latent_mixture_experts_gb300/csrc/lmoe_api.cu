@@ -955,6 +955,14 @@ static lmoe_status run_experts(lmoe_ctx* h, long long P, int BNm, int split, con
     p.wsc1 = static_cast<const float*>(h->w.ex_up_s);
     p.NB = ceil_div(h->F, 128);
     p.KB = ceil_div(dx, 128);
+    if (!h->fp8 && !h->fp4 && p.KS > 1) {
+      // a few tokens: the down weights of the first experts go to L2 while the gate/up pass drains
+      p.pf_codes = h->codes_down;
+      p.pf_code_bytes = static_cast<size_t>(dx) * (h->Fp / 2);
+      p.pf_atoms = h->sfa_down;
+      p.pf_atom_bytes = static_cast<size_t>(h->MTa_dn) * h->KG_dn * 512;
+      p.pf_budget = kDownPrefetchBytes;
+    }
     StageTimer tgu(h, LMOE_STAGE_EXPERT_GU, st);
     LMOE_TRY(h->fp8   ? launch_moe_fp8_gate_up(p, BNm, h->num_sms, st)
              : h->fp4 ? launch_moe_fp4_gate_up(p, BNm, h->num_sms, st)
@@ -962,6 +970,7 @@ static lmoe_status run_experts(lmoe_ctx* h, long long P, int BNm, int split, con
     ++launches;
     tgu.done();
     MoeGemmParams q = p;
+    q.pf_codes = nullptr;
     q.a_gate = h->m_exd[mi];
     if (h->fp4) {
       if (!map_u8(&q.b, h->hq, h->Fp / 2, static_cast<long long>(h->terms) * h->Ppad, b_rows)) return LMOE_ERR_CUDA;

@@ -216,7 +216,17 @@ struct MoeGemmParams {
   const float* wsc0;
   const float* wsc1;
   int NB, KB;
+  // K-split gate/up pass (MXFP4 weights): once a CTA has issued its last load
+  // it prefetches into L2 its share of the down-pass weights of the batch's
+  // experts, in the order the down pass takes them, up to pf_budget bytes
+  // (pf_codes null: no prefetch).  Sizes are multiples of 16 bytes.
+  const uint8_t* pf_codes;       // down codes, pf_code_bytes per expert
+  const uint8_t* pf_atoms;       // down scale atoms, pf_atom_bytes per expert
+  size_t pf_code_bytes, pf_atom_bytes, pf_budget;
 };
+// Down-pass weight bytes the K-split gate/up pass prefetches into L2: about
+// half of the 129 MB L2, so the prefetch does not evict its own first lines.
+constexpr size_t kDownPrefetchBytes = static_cast<size_t>(64) << 20;
 cudaError_t launch_moe_gate_up(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
 cudaError_t launch_moe_down(const MoeGemmParams& p, int BN, int grid, cudaStream_t s);
 // FP8 E4M3 weights with 128 x 128 fp32 block scales (BN 16 or 32).

@@ -174,6 +174,33 @@ __device__ __forceinline__ void ksplit_gate_up(const MoeGemmParams& p, uint32_t 
 constexpr int kScaleWarps = 4;
 constexpr int kMoeThreads = 64 + 32 * (kEpiWarps + kScaleWarps);   // TMA, MMA, epilogue x4, scales x4
 
+// L2 prefetch of the down-pass weights of the experts in the tile list: their
+// codes, then their scale atoms, expert by expert (the order in which the
+// down pass claims its items), cut into 32 KB chunks and cut off after
+// p.pf_budget bytes; this CTA takes chunks blockIdx.x, blockIdx.x + gridDim.x, ...
+__device__ __forceinline__ void prefetch_down_weights(const MoeGemmParams& p, int ntiles) {
+  constexpr size_t kChunk = 32768;
+  const size_t grid = gridDim.x;
+  size_t c0 = 0, used = 0;   // chunks and bytes of the ranges before the current one
+  for (int i = 0; i < ntiles && used < p.pf_budget; ++i) {
+    const int e = p.tiles[i].x;
+    if (i > 0 && p.tiles[i - 1].x == e) continue;   // an expert's tiles are adjacent
+    for (int r = 0; r < 2 && used < p.pf_budget; ++r) {
+      const uint8_t* base = r == 0 ? p.pf_codes + static_cast<size_t>(e) * p.pf_code_bytes
+                                   : p.pf_atoms + static_cast<size_t>(e) * p.pf_atom_bytes;
+      size_t len = r == 0 ? p.pf_code_bytes : p.pf_atom_bytes;
+      if (len > p.pf_budget - used) len = p.pf_budget - used;
+      const size_t n = (len + kChunk - 1) / kChunk;
+      for (size_t c = (blockIdx.x + grid - c0 % grid) % grid; c < n; c += grid) {
+        const size_t off = c * kChunk;
+        prefetch_l2_bulk(base + off, static_cast<uint32_t>(len - off < kChunk ? len - off : kChunk));
+      }
+      c0 += n;
+      used += len;
+    }
+  }
+}
+
 // KSP: the K-split form for small batches (p.KS splits per item); without it
 // p.KS is taken as 1.
 template <int BN, bool GU, bool KSP>
@@ -276,6 +303,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) moe_gemm_kernel(const __grid_c
         }
         w = nxt < total ? nxt : -1;
       }
+      // the down pass's weights stream into L2 while this pass drains
+      if constexpr (GU && KSP)
+        if (ok && p.pf_codes) prefetch_down_weights(p, ntiles);
     }
   } else if (warp == 1) {
     if (lane == 0) {
