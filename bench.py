@@ -53,9 +53,14 @@ UNIT = "tokens/s"
 # stands on a small case of the same instantiation (K3 shapes with 64
 # experts at T = 8: 702.2 MB for 645.2 MB; at T = 1024, the prefill tile:
 # 997.0 MB for 974 MB; K2 shapes with 32 experts at T = 384: 1033.2 MB for
-# 998.1 MB), keyed by (weight format, token tile).  An entry is removed when
+# 998.1 MB), keyed by (weight format, token tile, K-split form).  The K-split
+# form of one to a few tokens (K3 shapes with 64 experts at T = 1: 260.9 MB
+# for 187.4 MB) also prefetches 64 MiB of the batch's down weights into L2
+# for the down pass, which its DRAM bytes include.  An entry is removed when
 # its kernel changes until it is captured again.
-GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16): 1.088, ("mxfp4", 96): 1.024, ("fp8_block128", 96): 1.035}
+GU_DRAM_PER_ALGO_BYTE = {("mxfp4", 16, False): 1.088, ("mxfp4", 16, True): 1.392, ("mxfp4", 96, False): 1.024,
+                         ("fp8_block128", 96, False): 1.035}
+KSPLIT_MAX_P = 1024   # largest batch (assignments) the library considers for the K-split form
 
 
 def expert_tile(cfg, T: int) -> int:
@@ -66,6 +71,17 @@ def expert_tile(cfg, T: int) -> int:
         return 16 if P <= 4 * E else 32 if P <= 16 * E else 64 if P <= 64 * E else 96
     m = -(-P // E)
     return 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 96
+
+
+def gate_up_ksplit(cfg, T: int, num_sms: int = 152) -> bool:
+    """Whether the library runs the gate/up pass in its K-split form (the rule
+    of expert_ksplit in the library: MXFP4 weights, the 16-assignment tile and
+    fewer than two 256-row weight items per SM)."""
+    P, E = T * cfg.top_k, cfg.n_experts
+    if cfg.expert_wfmt != "mxfp4" or P > KSPLIT_MAX_P or expert_tile(cfg, T) != 16:
+        return False
+    tiles = min(P, P // 16 + min(E, P))
+    return tiles * -(-cfg.d_expert_ff // 256) < 2 * num_sms
 
 
 def _mat_bytes(cfg, N: int, K: int) -> int:
@@ -316,7 +332,7 @@ def gate_up_roofline(cfg, T: int, U: float, gu_ms: float, pk: dict, tc: dict | N
         r.update({"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                   "frac": round(achieved_gbs / pk["hbm"], 4),
                   "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs)"})
-    tr = None if e2m1 else GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T)))
+    tr = None if e2m1 else GU_DRAM_PER_ALGO_BYTE.get((cfg.expert_wfmt, expert_tile(cfg, T), gate_up_ksplit(cfg, T)))
     r["traffic"] = int(tr * gu_bytes) if tr else None
     r["traffic_source"] = ("ncu dram__bytes_read+write of this kernel on a small case of the same instantiation, "
                            "scaled to this launch by its algorithmic bytes" if tr else

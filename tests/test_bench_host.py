@@ -49,3 +49,14 @@ def test_expert_tile_rule():
     assert bench.expert_tile(C.K3, 8192) == 96
     assert bench.expert_tile(C.K2, 4096) == 96
     assert bench.expert_tile(C.workload("k2_e32_t384").cfg, 384) == 96
+
+
+def test_gate_up_ksplit_rule():
+    """bench.py's copy of the library's K-split rule: the full K3 layer splits
+    the gate/up pass at one token only (16 expert tiles x 12 weight items is
+    under two items per SM; two tokens may select 32 experts), the 64-expert
+    profiling case at one token, FP8 never."""
+    assert [t for t in range(1, 17) if bench.gate_up_ksplit(C.K3, t)] == [1]
+    assert bench.gate_up_ksplit(C.workload("k3_e64_t8").cfg, 1)
+    assert not bench.gate_up_ksplit(C.K3, 64)
+    assert not bench.gate_up_ksplit(C.K2, 1)
